@@ -1,0 +1,292 @@
+/*
+ * gqa_oracle.c -- plain, slow, fp64 CPU oracle for grouped-query attention
+ * forward and backward.  TEST INFRASTRUCTURE ONLY: only the test-suite, the
+ * smoke check and the benchmark's CPU-baseline leg may load this library.  It
+ * shares no code, header or constant with the CUDA path.
+ *
+ * What it computes (notation of the pages; h = query head, g = kv head,
+ * i = query row, j = key row, d = feature):
+ *
+ *   g          = h / (Hq / Hkv)                        ("bx // groups", tilelang
+ *                                                       PR #1093, Additional comments)
+ *   A(i)       = { j in the same sequence as i, j <= i if causal,
+ *                  i - j < W if a window W > 0 is set }
+ *   S_ij       = scale * sum_d Q[h,i,d] K[g,j,d]       (tilelang-ascend PR #1638,
+ *                                                       review thread, k1/k2)
+ *   LSE_i      = log( [e^{sink_h}] + sum_{j in A(i)} e^{S_ij} )
+ *                                                      (forward with attention sink,
+ *                                                       PR #1638 commit "4->2 kernels")
+ *   P_ij       = exp(S_ij - LSE_i),  p_sink_i = exp(sink_h - LSE_i)
+ *   O_i        = sum_j P_ij V[g,j]
+ *   Delta_i    = sum_d dO[h,i,d] O[h,i,d]              (PR #1638, Phase0(Delta))
+ *   dP_ij      = sum_d dO[h,i,d] V[g,j,d]              (PR #1638, k3)
+ *   dS_ij      = P_ij (dP_ij - Delta_i) * scale        (PR #1638, k4)
+ *   dQ_i       = sum_j dS_ij K[g,j]                    (PR #1638, k5)
+ *   dK_j       = sum_{h in group g} sum_i dS_ij Q[h,i] (PR #1638, k5; the group
+ *                                                       sum: PR #1093 comments)
+ *   dV_j       = sum_{h in group g} sum_i P_ij dO[h,i] (PR #1638, k3)
+ *   dsink_h    = - sum_{b,i} p_sink_i Delta_i          (PR #1638, "Kernel 9: Dsink")
+ *
+ * The sink is one extra logit per query head that enters the softmax
+ * denominator and has no value vector; it is in scaled-logit units.
+ *
+ * Layout: every tensor is dense row-major [B, H, S, D] in fp64 (S is the
+ * per-batch length, or the packed token count T when cu_seqlens is given, in
+ * which case B == 1).  LSE / Delta are [B, Hq, S].
+ *
+ * Evaluation order is the plain definition: a row pass over (b, h, i) and a
+ * column pass over (b, g, j) that revisits every (h, i) which sees key j, so no
+ * output is ever written by two threads.  OpenMP only splits independent rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+  int B, Hq, Hkv, S, Dqk, Dv;
+  int causal;          /* 1: key j visible to query i only if j <= i (top-left) */
+  int window;          /* > 0: additionally i - j < window; <= 0: no window */
+  double scale;        /* softmax scale applied to Q.K */
+  int nseq;            /* number of packed sequences when cu_seqlens != NULL */
+  const int32_t* cu_seqlens; /* [nseq+1] token offsets, or NULL (dense) */
+  const double* sink;  /* [Hq] or NULL */
+} oracle_problem;
+
+/* Range of key rows visible to query row i (both in absolute token index
+ * within the S axis), returned as [lo, hi) ; empty if lo >= hi. */
+static void key_range(const oracle_problem* p, int i, int* lo, int* hi) {
+  int s0 = 0, s1 = p->S;
+  if (p->cu_seqlens) {
+    for (int s = 0; s < p->nseq; ++s) {
+      if (i >= p->cu_seqlens[s] && i < p->cu_seqlens[s + 1]) {
+        s0 = p->cu_seqlens[s];
+        s1 = p->cu_seqlens[s + 1];
+        break;
+      }
+    }
+  }
+  int a = s0, b = s1;
+  if (p->causal && i + 1 < b) b = i + 1;
+  if (p->window > 0 && i - p->window + 1 > a) a = i - p->window + 1;
+  *lo = a;
+  *hi = b;
+}
+
+static inline const double* row(const double* t, int H, int S, int D, int b, int h, int i) {
+  return t + (((size_t)b * H + h) * S + i) * D;
+}
+
+static double dot(const double* x, const double* y, int n) {
+  double s = 0.0;
+  for (int d = 0; d < n; ++d) s += x[d] * y[d];
+  return s;
+}
+
+/* Scaled logit S_ij. */
+static double logit(const oracle_problem* p, const double* q, const double* k, int b, int h, int i, int j) {
+  const int g = h / (p->Hq / p->Hkv);
+  return p->scale * dot(row(q, p->Hq, p->S, p->Dqk, b, h, i), row(k, p->Hkv, p->S, p->Dqk, b, g, j), p->Dqk);
+}
+
+/* LSE_i from its definition, with the row maximum subtracted for stability. */
+static double row_lse(const oracle_problem* p, const double* q, const double* k, int b, int h, int i) {
+  int lo, hi;
+  key_range(p, i, &lo, &hi);
+  double m = -INFINITY;
+  if (p->sink) m = p->sink[h];
+  for (int j = lo; j < hi; ++j) {
+    double s = logit(p, q, k, b, h, i, j);
+    if (s > m) m = s;
+  }
+  if (m == -INFINITY) return -INFINITY;
+  double z = p->sink ? exp(p->sink[h] - m) : 0.0;
+  for (int j = lo; j < hi; ++j) z += exp(logit(p, q, k, b, h, i, j) - m);
+  return m + log(z);
+}
+
+/* Forward: O and LSE for every (b, h, i). */
+void oracle_forward(const oracle_problem* p, const double* q, const double* k, const double* v, double* o,
+                    double* lse) {
+  const int G = p->Hq / p->Hkv;
+  const long nrows = (long)p->B * p->Hq * p->S;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long r = 0; r < nrows; ++r) {
+    const int i = (int)(r % p->S), h = (int)((r / p->S) % p->Hq), b = (int)(r / ((long)p->S * p->Hq));
+    const int g = h / G;
+    const double L = row_lse(p, q, k, b, h, i);
+    lse[r] = L;
+    double* orow = o + (size_t)r * p->Dv;
+    for (int d = 0; d < p->Dv; ++d) orow[d] = 0.0;
+    int lo, hi;
+    key_range(p, i, &lo, &hi);
+    for (int j = lo; j < hi; ++j) {
+      const double pij = exp(logit(p, q, k, b, h, i, j) - L);
+      const double* vj = row(v, p->Hkv, p->S, p->Dv, b, g, j);
+      for (int d = 0; d < p->Dv; ++d) orow[d] += pij * vj[d];
+    }
+  }
+}
+
+/* Delta_i = rowsum(dO * O) for every row. */
+void oracle_delta(const oracle_problem* p, const double* o, const double* dout, double* delta) {
+  const long nrows = (long)p->B * p->Hq * p->S;
+#pragma omp parallel for schedule(static)
+  for (long r = 0; r < nrows; ++r) delta[r] = dot(dout + (size_t)r * p->Dv, o + (size_t)r * p->Dv, p->Dv);
+}
+
+/* dS_ij (with the scale) given the row statistics LSE_i and Delta_i. */
+static double grad_logit(const oracle_problem* p, const double* q, const double* k, const double* v,
+                         const double* dout, double L, double D_i, int b, int h, int i, int j, double* pij_out) {
+  const int g = h / (p->Hq / p->Hkv);
+  const double pij = exp(logit(p, q, k, b, h, i, j) - L);
+  const double dpij = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), row(v, p->Hkv, p->S, p->Dv, b, g, j), p->Dv);
+  if (pij_out) *pij_out = pij;
+  return pij * (dpij - D_i) * p->scale;
+}
+
+/*
+ * Backward.  Inputs: q, k, v, dout, and the forward's lse and o (Delta is
+ * formed from o and dout).  Outputs: delta [B,Hq,S], dq [B,Hq,S,Dqk],
+ * dk [B,Hkv,S,Dqk], dv [B,Hkv,S,Dv], dsink [Hq] (only if p->sink).
+ */
+void oracle_backward(const oracle_problem* p, const double* q, const double* k, const double* v,
+                     const double* o, const double* lse, const double* dout, double* delta, double* dq,
+                     double* dk, double* dv, double* dsink) {
+  const int G = p->Hq / p->Hkv;
+  oracle_delta(p, o, dout, delta);
+  const long nrows = (long)p->B * p->Hq * p->S;
+
+  /* row pass: dQ_i */
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long r = 0; r < nrows; ++r) {
+    const int i = (int)(r % p->S), h = (int)((r / p->S) % p->Hq), b = (int)(r / ((long)p->S * p->Hq));
+    const int g = h / G;
+    double* dqi = dq + (size_t)r * p->Dqk;
+    for (int d = 0; d < p->Dqk; ++d) dqi[d] = 0.0;
+    int lo, hi;
+    key_range(p, i, &lo, &hi);
+    for (int j = lo; j < hi; ++j) {
+      const double ds = grad_logit(p, q, k, v, dout, lse[r], delta[r], b, h, i, j, NULL);
+      const double* kj = row(k, p->Hkv, p->S, p->Dqk, b, g, j);
+      for (int d = 0; d < p->Dqk; ++d) dqi[d] += ds * kj[d];
+    }
+  }
+
+  /* column pass: dK_j, dV_j summed over every query head of the group */
+  const long ncols = (long)p->B * p->Hkv * p->S;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long c = 0; c < ncols; ++c) {
+    const int j = (int)(c % p->S), g = (int)((c / p->S) % p->Hkv), b = (int)(c / ((long)p->S * p->Hkv));
+    double* dkj = dk + (size_t)c * p->Dqk;
+    double* dvj = dv + (size_t)c * p->Dv;
+    for (int d = 0; d < p->Dqk; ++d) dkj[d] = 0.0;
+    for (int d = 0; d < p->Dv; ++d) dvj[d] = 0.0;
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      for (int i = 0; i < p->S; ++i) {
+        int lo, hi;
+        key_range(p, i, &lo, &hi);
+        if (j < lo || j >= hi) continue;
+        const long r = ((long)b * p->Hq + h) * p->S + i;
+        double pij;
+        const double ds = grad_logit(p, q, k, v, dout, lse[r], delta[r], b, h, i, j, &pij);
+        const double* qi = row(q, p->Hq, p->S, p->Dqk, b, h, i);
+        const double* doi = row(dout, p->Hq, p->S, p->Dv, b, h, i);
+        for (int d = 0; d < p->Dqk; ++d) dkj[d] += ds * qi[d];
+        for (int d = 0; d < p->Dv; ++d) dvj[d] += pij * doi[d];
+      }
+    }
+  }
+
+  /* dsink_h = - sum over b, i of p_sink_i * Delta_i */
+  if (p->sink && dsink) {
+    for (int h = 0; h < p->Hq; ++h) {
+      double acc = 0.0;
+      for (int b = 0; b < p->B; ++b)
+        for (int i = 0; i < p->S; ++i) {
+          const long r = ((long)b * p->Hq + h) * p->S + i;
+          acc += exp(p->sink[h] - lse[r]) * delta[r];
+        }
+      dsink[h] = -acc;
+    }
+  }
+}
+
+/*
+ * Sampled evaluation for problems too large for the full passes.
+ *
+ * Query side: for each listed (b, h, i) it computes LSE_i, O_i, Delta_i and
+ * dQ_i exactly (Delta from its own O).  Outputs are packed in list order:
+ * lse[n], o[n*Dv], delta[n], dq[n*Dqk].
+ *
+ * Key side: for each listed (b, g, j) it computes dK_j and dV_j exactly.  Each
+ * query row that sees j needs its own LSE and Delta, which are recomputed from
+ * the definition here (so the cost grows with the number of such rows).
+ */
+void oracle_sample_rows(const oracle_problem* p, const double* q, const double* k, const double* v,
+                        const double* dout, int n, const int32_t* bs, const int32_t* hs, const int32_t* is,
+                        double* lse, double* o, double* delta, double* dq) {
+  const int G = p->Hq / p->Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    const int b = bs[t], h = hs[t], i = is[t], g = h / G;
+    const double L = row_lse(p, q, k, b, h, i);
+    double* orow = o + (size_t)t * p->Dv;
+    for (int d = 0; d < p->Dv; ++d) orow[d] = 0.0;
+    int lo, hi;
+    key_range(p, i, &lo, &hi);
+    for (int j = lo; j < hi; ++j) {
+      const double pij = exp(logit(p, q, k, b, h, i, j) - L);
+      const double* vj = row(v, p->Hkv, p->S, p->Dv, b, g, j);
+      for (int d = 0; d < p->Dv; ++d) orow[d] += pij * vj[d];
+    }
+    const double Di = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), orow, p->Dv);
+    lse[t] = L;
+    delta[t] = Di;
+    double* dqi = dq + (size_t)t * p->Dqk;
+    for (int d = 0; d < p->Dqk; ++d) dqi[d] = 0.0;
+    for (int j = lo; j < hi; ++j) {
+      const double ds = grad_logit(p, q, k, v, dout, L, Di, b, h, i, j, NULL);
+      const double* kj = row(k, p->Hkv, p->S, p->Dqk, b, g, j);
+      for (int d = 0; d < p->Dqk; ++d) dqi[d] += ds * kj[d];
+    }
+  }
+}
+
+void oracle_sample_cols(const oracle_problem* p, const double* q, const double* k, const double* v,
+                        const double* dout, int n, const int32_t* bs, const int32_t* gs, const int32_t* js,
+                        double* dk, double* dv) {
+  const int G = p->Hq / p->Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    const int b = bs[t], g = gs[t], j = js[t];
+    double* dkj = dk + (size_t)t * p->Dqk;
+    double* dvj = dv + (size_t)t * p->Dv;
+    for (int d = 0; d < p->Dqk; ++d) dkj[d] = 0.0;
+    for (int d = 0; d < p->Dv; ++d) dvj[d] = 0.0;
+    double* orow = (double*)malloc(sizeof(double) * (size_t)p->Dv);
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      for (int i = 0; i < p->S; ++i) {
+        int lo, hi;
+        key_range(p, i, &lo, &hi);
+        if (j < lo || j >= hi) continue;
+        /* this query row's own statistics, from the definition */
+        const double L = row_lse(p, q, k, b, h, i);
+        for (int d = 0; d < p->Dv; ++d) orow[d] = 0.0;
+        for (int jj = lo; jj < hi; ++jj) {
+          const double pw = exp(logit(p, q, k, b, h, i, jj) - L);
+          const double* vj = row(v, p->Hkv, p->S, p->Dv, b, g, jj);
+          for (int d = 0; d < p->Dv; ++d) orow[d] += pw * vj[d];
+        }
+        const double Di = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), orow, p->Dv);
+        double pij;
+        const double ds = grad_logit(p, q, k, v, dout, L, Di, b, h, i, j, &pij);
+        const double* qi = row(q, p->Hq, p->S, p->Dqk, b, h, i);
+        const double* doi = row(dout, p->Hq, p->S, p->Dv, b, h, i);
+        for (int d = 0; d < p->Dqk; ++d) dkj[d] += ds * qi[d];
+        for (int d = 0; d < p->Dv; ++d) dvj[d] += pij * doi[d];
+      }
+    }
+    free(orow);
+  }
+}
