@@ -1,0 +1,85 @@
+"""GB300 (sm_103a) grouped-query FlashAttention forward and backward.
+
+The computation lives in ``libgqa_attn.so`` (hand-written CUDA behind the C ABI
+of ``include/gqa_attn.h``); this package only marshals PyTorch device tensors
+into those calls.  The two helpers below chain the entry points in the order
+the C ABI prescribes:
+
+* :func:`attention_forward`  -> ``gqa_attn_fwd``
+* :func:`attention_backward` -> ``gqa_attn_bwd_preprocess``, ``gqa_attn_bwd``,
+  ``gqa_attn_bwd_postprocess`` and (with a sink) ``gqa_attn_dsink``.
+
+Tensors use the BHSD layout: q [B,Hq,S,Dqk], k [B,Hkv,S,Dqk], v [B,Hkv,S,Dv],
+o/dout [B,Hq,S,Dv]; packed variable-length batches use B=1 and ``cu_seqlens``.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _native as native
+from ._native import (GQA_GROUP_ATOMIC, GQA_GROUP_TMEM, GQA_RED_BULK, GQA_RED_NONE, GQA_RED_SCALAR,
+                      GQA_RED_V4, GqaError)
+
+__all__ = [
+    "attention_forward", "attention_backward", "native", "GqaError", "GQA_GROUP_TMEM", "GQA_GROUP_ATOMIC",
+    "GQA_RED_V4", "GQA_RED_BULK", "GQA_RED_SCALAR", "GQA_RED_NONE",
+]
+
+
+def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=GQA_GROUP_TMEM,
+            red_mode=GQA_RED_V4, deterministic=False):
+    B, Hq, S, Dqk = q.shape
+    Hkv, Dv = k.shape[1], v.shape[3]
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype):
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+    return native.make_params(B, Hq, Hkv, S, Dqk, Dv, q.dtype, causal=causal, window=window, scale=scale,
+                              cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, group_mode=group_mode,
+                              red_mode=red_mode, deterministic=deterministic)
+
+
+def attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = True, window: int = 0,
+                      scale: Optional[float] = None, sink: Optional[torch.Tensor] = None,
+                      cu_seqlens: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
+                      workspace: Optional[torch.Tensor] = None):
+    """Returns (o, lse): o [B,Hq,S,Dv] in q's dtype, lse [B,Hq,S] fp32 (natural log, sink included)."""
+    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen)
+    B, Hq, S, _ = q.shape
+    o = torch.empty((B, Hq, S, v.shape[3]), dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    ws = workspace if workspace is not None else native.alloc_workspace(p, q.device)
+    native.fwd(p, q, k, v, sink, o, lse, ws)
+    return o, lse
+
+
+def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+                       dout: torch.Tensor, *, causal: bool = True, window: int = 0, scale: Optional[float] = None,
+                       sink: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                       max_seqlen: Optional[int] = None, group_mode: int = GQA_GROUP_TMEM,
+                       red_mode: int = GQA_RED_V4, deterministic: bool = False,
+                       workspace: Optional[torch.Tensor] = None, out: Optional[dict] = None) -> dict:
+    """Returns dict(dq, dk, dv, delta[, dsink]).  `out` may hold preallocated tensors of the same names."""
+    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode, red_mode, deterministic)
+    B, Hq, S, Dqk = q.shape
+    Hkv, Dv = k.shape[1], v.shape[3]
+    res = dict(out) if out else {}
+    dev = q.device
+    if "dq" not in res:
+        res["dq"] = torch.empty_like(q)
+    if "dk" not in res:
+        res["dk"] = torch.empty_like(k)
+    if "dv" not in res:
+        res["dv"] = torch.empty_like(v)
+    if "delta" not in res:
+        res["delta"] = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    if sink is not None and "dsink" not in res:
+        res["dsink"] = torch.empty((Hq,), dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else native.alloc_workspace(p, dev)
+    native.bwd_preprocess(p, o, dout, lse, res["delta"], ws)
+    native.bwd(p, q, k, v, dout, res["dq"], res["dk"], res["dv"], ws)
+    native.bwd_postprocess(p, res["dq"], res["dk"], res["dv"], ws)
+    if sink is not None:
+        native.dsink(p, sink, lse, res["delta"], res["dsink"])
+    return res

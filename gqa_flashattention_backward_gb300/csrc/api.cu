@@ -1,0 +1,317 @@
+// C-ABI entry points of libgqa_attn.so: argument validation, workspace layout,
+// TMA tensor-map construction and kernel launches.  See include/gqa_attn.h for
+// the contract of each call.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "../../include/gqa_attn.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace gqa {
+bool kv_kernel_has_dq(int Dqk);
+bool kv_kernel_has_bulk_dq(int Dqk);
+int kv_kernel_bq(int Dqk);
+}  // namespace gqa
+
+using namespace gqa;
+
+namespace {
+
+constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clock
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_dims(int dqk, int dv) {
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
+}
+
+gqa_status validate(const gqa_attn_params* p) {
+  if (!p) return GQA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->S < 0) return GQA_ERR_INVALID_ARG;
+  if (p->Hq % p->Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (p->dtype != GQA_F16 && p->dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return GQA_ERR_INVALID_ARG;
+  if (p->window > 0 && !p->causal) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale) || !(p->scale > 0.f)) return GQA_ERR_INVALID_ARG;
+  if (p->group_mode != GQA_GROUP_TMEM && p->group_mode != GQA_GROUP_ATOMIC) return GQA_ERR_INVALID_ARG;
+  if (p->red_mode < GQA_RED_V4 || p->red_mode > GQA_RED_NONE) return GQA_ERR_INVALID_ARG;
+  if (p->deterministic != 0 && p->deterministic != 1) return GQA_ERR_INVALID_ARG;
+  if (p->cu_seqlens) {
+    if (p->B != 1 || p->nseq < 1 || p->nseq > 65535) return GQA_ERR_INVALID_ARG;
+    if (p->max_seqlen < 1 || (p->S > 0 && p->max_seqlen > p->S)) return GQA_ERR_INVALID_ARG;
+    if (!aligned(p->cu_seqlens, 4)) return GQA_ERR_INVALID_ARG;
+  } else if (p->B > 65535) {
+    return GQA_ERR_INVALID_ARG;
+  }
+  const long long max_len = p->cu_seqlens ? p->max_seqlen : p->S;
+  if ((max_len + 127) / 128 > 65535) return GQA_ERR_UNSUPPORTED;
+  if (!supported_dims(p->Dqk, p->Dv)) return GQA_ERR_UNSUPPORTED;
+  // bulk dQ reduction needs shared-memory staging, which only the d=64 tile has room for
+  if (!p->deterministic && p->red_mode == GQA_RED_BULK && kv_kernel_has_dq(p->Dqk) && !kv_kernel_has_bulk_dq(p->Dqk))
+    return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+struct Derived {
+  Problem pr;
+  WsLayout ws;
+  bool need_dq_acc, need_dkdv_acc, group_tmem;
+};
+
+Derived derive(const gqa_attn_params* p, void* ws) {
+  Derived d{};
+  d.group_tmem = p->deterministic || p->group_mode == GQA_GROUP_TMEM;
+  d.need_dq_acc = !p->deterministic && kv_kernel_has_dq(p->Dqk);
+  d.need_dkdv_acc = !d.group_tmem;
+  Problem& pr = d.pr;
+  pr.B = p->B;
+  pr.Hq = p->Hq;
+  pr.Hkv = p->Hkv;
+  pr.S = p->S;
+  pr.Dqk = p->Dqk;
+  pr.Dv = p->Dv;
+  pr.G = p->Hq / p->Hkv;
+  pr.causal = p->causal;
+  pr.window = p->window > 0 ? p->window : 0;
+  pr.scale = p->scale;
+  pr.scale_log2 = p->scale * kLog2e;
+  pr.cu_seqlens = p->cu_seqlens;
+  pr.nseqs = p->cu_seqlens ? p->nseq : p->B;
+  pr.max_len = p->cu_seqlens ? p->max_seqlen : p->S;
+  pr.ntiles = (pr.max_len + kStatTile - 1) / kStatTile;
+  pr.wait_limit = g_wait_limit.load();
+  d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc, d.need_dkdv_acc);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  pr.err = reinterpret_cast<int*>(base + d.ws.err_off);
+  pr.lse2 = reinterpret_cast<float*>(base + d.ws.lse2_off);
+  pr.delta_t = reinterpret_cast<float*>(base + d.ws.delta_off);
+  pr.dq_acc = d.need_dq_acc ? reinterpret_cast<float*>(base + d.ws.dq_off) : nullptr;
+  pr.dk_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dk_off) : nullptr;
+  pr.dv_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dv_off) : nullptr;
+  return d;
+}
+
+gqa_status check_ws(const gqa_attn_params* p, void* ws, size_t bytes) {
+  if (!ws || !aligned(ws, 256)) return GQA_ERR_WORKSPACE;
+  if (bytes < gqa_attn_workspace_size(p)) return GQA_ERR_WORKSPACE;
+  return GQA_OK;
+}
+
+bool map16(CUtensorMap* m, const void* ptr, int D, int S, int Z, int box_rows, bool bf16) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(Z)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map32(CUtensorMap* m, const float* ptr, int D, int S, int Z) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(Z)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(S) * D * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+gqa_status to_status(cudaError_t e) { return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t gqa_attn_workspace_size(const gqa_attn_params* p) {
+  if (validate(p) != GQA_OK) return 0;
+  return derive(p, nullptr).ws.total;
+}
+
+gqa_status gqa_attn_fwd(const gqa_attn_params* p, const void* q, const void* k, const void* v, const float* sink,
+                        void* o, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  gqa_status s = validate(p);
+  if (s != GQA_OK) return s;
+  if ((s = check_ws(p, workspace, ws_bytes)) != GQA_OK) return s;
+  if (!q || !k || !v || !o || !lse) return GQA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (sink && !aligned(sink, 4)))
+    return GQA_ERR_INVALID_ARG;
+  if (p->S == 0) return GQA_OK;
+  Derived d = derive(p, workspace);
+  const bool bf = p->dtype == GQA_BF16;
+  Maps m;
+  std::memset(&m, 0, sizeof(m));
+  if (!map16(&m.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) || !map16(&m.k, k, p->Dqk, p->S, p->B * p->Hkv, 128, bf) ||
+      !map16(&m.v, v, p->Dv, p->S, p->B * p->Hkv, 128, bf))
+    return GQA_ERR_CUDA;
+  return to_status(launch_fwd(d.pr, bf, m, sink, o, lse, static_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_bwd_preprocess(const gqa_attn_params* p, const void* o, const void* dout, const float* lse,
+                                   float* delta, void* workspace, size_t ws_bytes, void* stream) {
+  gqa_status s = validate(p);
+  if (s != GQA_OK) return s;
+  if ((s = check_ws(p, workspace, ws_bytes)) != GQA_OK) return s;
+  if (!o || !dout || !lse || !delta) return GQA_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(lse, 4) || !aligned(delta, 4)) return GQA_ERR_INVALID_ARG;
+  if (p->S == 0) return GQA_OK;
+  Derived d = derive(p, workspace);
+  return to_status(launch_preprocess(d.pr, p->dtype == GQA_BF16, o, dout, lse, delta, d.need_dq_acc,
+                                     d.need_dkdv_acc, num_sms(), static_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_bwd(const gqa_attn_params* p, const void* q, const void* k, const void* v, const void* dout,
+                        void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
+  gqa_status s = validate(p);
+  if (s != GQA_OK) return s;
+  if ((s = check_ws(p, workspace, ws_bytes)) != GQA_OK) return s;
+  Derived d = derive(p, workspace);
+  const bool dq_pass = !d.need_dq_acc;  // deterministic, or dims whose dQ always comes from that pass
+  if (!q || !k || !v || !dout) return GQA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16)) return GQA_ERR_INVALID_ARG;
+  if (dq_pass && (!dq || !aligned(dq, 16))) return GQA_ERR_INVALID_ARG;
+  if (d.group_tmem && (!dk || !dv || !aligned(dk, 16) || !aligned(dv, 16))) return GQA_ERR_INVALID_ARG;
+  if (p->S == 0) return GQA_OK;
+  const bool bf = p->dtype == GQA_BF16;
+  const int bq = kv_kernel_bq(p->Dqk);
+  Maps m;
+  std::memset(&m, 0, sizeof(m));
+  if (!map16(&m.q, q, p->Dqk, p->S, p->B * p->Hq, bq, bf) || !map16(&m.dout, dout, p->Dv, p->S, p->B * p->Hq, bq, bf) ||
+      !map16(&m.k, k, p->Dqk, p->S, p->B * p->Hkv, 128, bf) || !map16(&m.v, v, p->Dv, p->S, p->B * p->Hkv, 128, bf))
+    return GQA_ERR_CUDA;
+  if (d.need_dq_acc && !map32(&m.dq_acc, d.pr.dq_acc, p->Dqk, p->S, p->B * p->Hq)) return GQA_ERR_CUDA;
+  if (d.need_dkdv_acc && (!map32(&m.dk_acc, d.pr.dk_acc, p->Dqk, p->S, p->B * p->Hkv) ||
+                          !map32(&m.dv_acc, d.pr.dv_acc, p->Dv, p->S, p->B * p->Hkv)))
+    return GQA_ERR_CUDA;
+  static const int red_to_mode[4] = {kDqRedV4, kDqBulk, kDqScalar, kDqStore};
+  KvLaunch kl;
+  kl.group_tmem = d.group_tmem ? 1 : 0;
+  kl.dq_mode = d.need_dq_acc ? red_to_mode[p->red_mode] : kDqNone;
+  kl.kv_red_mode = red_to_mode[p->red_mode];
+  kl.dk = dk;
+  kl.dv = dv;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_kv(d.pr, bf, m, kl, st);
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
+  if (dq_pass) {
+    Maps m2 = m;
+    if (bq != 128 && (!map16(&m2.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) ||
+                      !map16(&m2.dout, dout, p->Dv, p->S, p->B * p->Hq, 128, bf)))
+      return GQA_ERR_CUDA;
+    e = launch_dq(d.pr, bf, m2, dq, st);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+
+gqa_status gqa_attn_bwd_postprocess(const gqa_attn_params* p, void* dq, void* dk, void* dv, void* workspace,
+                                    size_t ws_bytes, void* stream) {
+  gqa_status s = validate(p);
+  if (s != GQA_OK) return s;
+  if ((s = check_ws(p, workspace, ws_bytes)) != GQA_OK) return s;
+  Derived d = derive(p, workspace);
+  if (d.need_dq_acc && (!dq || !aligned(dq, 16))) return GQA_ERR_INVALID_ARG;
+  if (d.need_dkdv_acc && (!dk || !dv || !aligned(dk, 16) || !aligned(dv, 16))) return GQA_ERR_INVALID_ARG;
+  if (p->S == 0) return GQA_OK;
+  const bool bf = p->dtype == GQA_BF16;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = num_sms();
+  if (d.need_dq_acc) {
+    cudaError_t e = launch_cast(d.pr.dq_acc, dq, static_cast<long long>(p->B) * p->Hq * p->S * p->Dqk, p->scale, bf,
+                                sms, st);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  if (d.need_dkdv_acc) {
+    const long long rows = static_cast<long long>(p->B) * p->Hkv * p->S;
+    cudaError_t e = launch_cast(d.pr.dk_acc, dk, rows * p->Dqk, p->scale, bf, sms, st);
+    if (e == cudaSuccess) e = launch_cast(d.pr.dv_acc, dv, rows * p->Dv, 1.f, bf, sms, st);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+
+gqa_status gqa_attn_dsink(const gqa_attn_params* p, const float* sink, const float* lse, const float* delta,
+                          float* dsink, void* stream) {
+  gqa_status s = validate(p);
+  if (s != GQA_OK) return s;
+  if (!sink || !lse || !delta || !dsink) return GQA_ERR_INVALID_ARG;
+  if (!aligned(sink, 4) || !aligned(lse, 4) || !aligned(delta, 4) || !aligned(dsink, 4)) return GQA_ERR_INVALID_ARG;
+  return to_status(launch_dsink(p->B, p->Hq, p->S, sink, lse, delta, dsink, static_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_get_device_error(void* workspace, size_t ws_bytes, void* stream, int* site) {
+  if (site) *site = 0;
+  if (!workspace || ws_bytes < 256 || !aligned(workspace, 256)) return GQA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GQA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GQA_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  if (site) *site = word;
+  if (word == 0) return GQA_OK;
+  if (static_cast<unsigned>(word) & 0x80000000u) return GQA_ERR_DEVICE_TIMEOUT;
+  return GQA_ERR_DEVICE_INPUT;
+}
+
+void gqa_attn_set_wait_limit(long long cycles) {
+  g_wait_limit.store(cycles > 0 ? cycles : kDefaultWaitLimit);
+}
+
+gqa_status gqa_attn_selftest_wait_timeout(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || ws_bytes < 256 || !aligned(workspace, 256)) return GQA_ERR_WORKSPACE;
+  return to_status(
+      launch_selftest_wait(static_cast<int*>(workspace), g_wait_limit.load(), static_cast<cudaStream_t>(stream)));
+}
+
+const char* gqa_attn_strerror(gqa_status s) {
+  switch (s) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported problem";
+    case GQA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case GQA_ERR_CUDA: return "CUDA error";
+    case GQA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    case GQA_ERR_DEVICE_INPUT: return "device-side input check failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// Shared definitions of the CUDA path: the problem descriptor handed to every
+// kernel, the workspace layout, and sequence/tile bookkeeping.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kStatTile = 128;  // row statistics are stored in blocks of 128 query rows
+
+// Error-word codes (low bits); bit 31 marks a timed-out wait.
+enum : int {
+  kErrSeqTooLong = 0x40000001,
+  kErrBadSeqlens = 0x40000002,
+};
+
+// Everything a kernel needs to know about the attention problem.
+struct Problem {
+  int B, Hq, Hkv, S, Dqk, Dv, G;  // G = Hq / Hkv
+  int causal, window;
+  float scale;        // softmax scale
+  float scale_log2;   // scale * log2(e): logits are exponentiated with ex2
+  const int32_t* cu_seqlens;  // device [nseqs+1] or null (dense)
+  int nseqs;          // packed sequences, or B when dense
+  int max_len;        // longest sequence (S when dense)
+  int ntiles;         // ceil(max_len / 128): stat tiles per (head, sequence)
+  int* err;           // device error word (workspace)
+  long long wait_limit;
+  // workspace regions
+  float* lse2;        // [Hq][nseqs][ntiles][128]  LSE * log2(e), +inf on padding rows
+  float* delta_t;     // same layout, Delta, 0 on padding rows
+  float* dq_acc;      // [B][Hq][S][Dqk] fp32
+  float* dk_acc;      // [B][Hkv][S][Dqk] fp32
+  float* dv_acc;      // [B][Hkv][S][Dv] fp32
+};
+
+// One sequence of the (possibly packed) batch.
+struct Seq {
+  int b;      // batch index (0 when packed)
+  int start;  // first token on the S axis
+  int len;    // tokens
+};
+
+__device__ __forceinline__ bool load_seq(const Problem& p, int s, Seq& q) {
+  if (p.cu_seqlens) {
+    const int a = __ldg(p.cu_seqlens + s), e = __ldg(p.cu_seqlens + s + 1);
+    q.b = 0;
+    q.start = a;
+    q.len = e - a;
+    if (q.len < 0 || a < 0 || e > p.S) {
+      atomicCAS(p.err, 0, kErrBadSeqlens);
+      q.len = 0;
+      return false;
+    }
+    if (q.len > p.max_len) {
+      atomicCAS(p.err, 0, kErrSeqTooLong);
+      q.len = 0;
+      return false;
+    }
+  } else {
+    q.b = s;
+    q.start = 0;
+    q.len = p.S;
+  }
+  return true;
+}
+
+// Index of the first float of a stats tile: head h, sequence s, 128-row tile t.
+__host__ __device__ __forceinline__ size_t stat_index(const Problem& p, int h, int s, int t) {
+  return ((static_cast<size_t>(h) * p.nseqs + s) * p.ntiles + t) * kStatTile;
+}
+
+// ---------------------------------------------------------------- workspace
+struct WsLayout {
+  size_t err_off, lse2_off, delta_off, dq_off, dk_off, dv_off, total;
+};
+
+__host__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Dqk, int Dv, int nseqs, int ntiles,
+                                   bool need_dq_acc, bool need_dkdv_acc) {
+  WsLayout w{};
+  size_t off = 0;
+  w.err_off = off;
+  off += 256;
+  const size_t nstat = static_cast<size_t>(Hq) * nseqs * ntiles * kStatTile;
+  w.lse2_off = off;
+  off = align256(off + nstat * 4);
+  w.delta_off = off;
+  off = align256(off + nstat * 4);
+  w.dq_off = off;
+  if (need_dq_acc) off = align256(off + static_cast<size_t>(B) * Hq * S * Dqk * 4);
+  w.dk_off = off;
+  if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * S * Dqk * 4);
+  w.dv_off = off;
+  if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * S * Dv * 4);
+  w.total = off;
+  return w;
+}
+
+// ---------------------------------------------------------------- tile ranges
+// Query rows i (local to the sequence) that can see some key of the 128-row
+// KV tile kt, as a range of query tiles of `bq` rows: [*t0, *t1).
+__host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len, int bq, int causal, int window,
+                                                             int* t0, int* t1) {
+  const int ntq = (len + bq - 1) / bq;
+  if (!causal) {
+    *t0 = 0;
+    *t1 = ntq;
+    return;
+  }
+  const int j_lo = kt * 128;
+  int a = j_lo / bq;
+  int b = ntq;
+  if (window > 0) {
+    const long long i_hi = static_cast<long long>(j_lo) + 127 + window - 1;  // last row seeing key j_lo+127
+    const long long tb = i_hi / bq + 1;
+    if (tb < b) b = static_cast<int>(tb);
+  }
+  *t0 = a;
+  *t1 = b > a ? b : a;
+}
+
+// Key tiles (128 rows) visible to the query tile qt of 128 rows: [*k0, *k1).
+__host__ __device__ __forceinline__ void kv_tiles_for_q_tile(int qt, int len, int causal, int window, int* k0,
+                                                             int* k1) {
+  const int ntk = (len + 127) / 128;
+  if (!causal) {
+    *k0 = 0;
+    *k1 = ntk;
+    return;
+  }
+  const int i_lo = qt * 128, i_hi = qt * 128 + 127;
+  int b = i_hi / 128 + 1;
+  if (b > ntk) b = ntk;
+  int a = 0;
+  if (window > 0) {
+    const int j_lo = i_lo - window + 1;
+    a = j_lo > 0 ? j_lo / 128 : 0;
+  }
+  *k0 = a;
+  *k1 = b > a ? b : a;
+}
+
+}  // namespace gqa

@@ -1,0 +1,225 @@
+// Memory-bound kernels of the backward path:
+//   preprocess  : Delta_i = sum_d dO_id * O_id; tiled row statistics for the
+//                 main kernels; zero the fp32 accumulators.
+//                 (tilelang-ascend PR #1638 "Add GQA Sink Backward BHSD": the
+//                 9->6 commit's preprocess kernel; Phase0(Delta) = sum(O*dO).)
+//   postprocess : fp32 accumulators -> fp16/bf16 outputs (dual-output cast of the
+//                 same PR's 9->6 commit; the 4->2 commit's "fp32 atomic_add
+//                 then cast").
+//   dsink       : dsink_h = -sum_{b,i} exp(sink_h - lse) * Delta ("Kernel 9: Dsink").
+// All are grid-stride kernels sized to a multiple of the SM count with 16-byte
+// vector accesses.
+#include "common.cuh"
+#include "umma.cuh"
+#include <type_traits>
+#include "launch.h"
+
+namespace gqa {
+
+template <typename T>
+__device__ __forceinline__ float2 to_f2(uint32_t u);
+template <>
+__device__ __forceinline__ float2 to_f2<__half>(uint32_t u) {
+  return __half22float2(*reinterpret_cast<__half2*>(&u));
+}
+template <>
+__device__ __forceinline__ float2 to_f2<__nv_bfloat16>(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+}
+
+// Locate sequence s and local index of token `row` on the S axis (packed case).
+__device__ __forceinline__ int find_seq(const int32_t* cu, int nseqs, int row) {
+  int lo = 0, hi = nseqs - 1;  // largest s with cu[s] <= row, among non-empty candidates
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  // skip empty sequences that share the same start
+  while (lo + 1 < nseqs && __ldg(cu + lo + 1) <= row) ++lo;
+  return lo;
+}
+
+// 8 threads per row; each thread covers Dv/8 elements.
+template <typename T, int DV>
+__global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __restrict__ o,
+                                                         const T* __restrict__ dout, const float* __restrict__ lse,
+                                                         float* __restrict__ delta, int zero_dq, int zero_dkdv) {
+  constexpr int PER = DV / 8;        // elements per thread
+  constexpr int VEC = PER / 8;       // uint4 loads per thread per tensor
+  const long long nrows = static_cast<long long>(p.B) * p.Hq * p.S;
+  const int sub = threadIdx.x & 7;
+  const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 3);
+  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 3) + (threadIdx.x >> 3); r < nrows;
+       r += stride) {
+    const uint4* po = reinterpret_cast<const uint4*>(o + r * DV + sub * PER);
+    const uint4* pd = reinterpret_cast<const uint4*>(dout + r * DV + sub * PER);
+    float acc = 0.f;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      const uint4 a = __ldg(po + v), b = __ldg(pd + v);
+      const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = to_f2<T>(aa[e]), y = to_f2<T>(bb[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    const int i = static_cast<int>(r % p.S);
+    const int h = static_cast<int>((r / p.S) % p.Hq);
+    const int b = static_cast<int>(r / (static_cast<long long>(p.S) * p.Hq));
+    int s, il, len;
+    if (p.cu_seqlens) {
+      s = find_seq(p.cu_seqlens, p.nseqs, i);
+      const int st = __ldg(p.cu_seqlens + s);
+      il = i - st;
+      len = __ldg(p.cu_seqlens + s + 1) - st;
+    } else {
+      s = b;
+      il = i;
+      len = p.S;
+    }
+    const bool ok = len <= p.max_len;
+    if (sub == 0) {
+      delta[r] = acc;
+      if (ok) {
+        const size_t base = stat_index(p, h, s, il / kStatTile) + (il % kStatTile);
+        p.lse2[base] = __ldg(lse + r) * kLog2e;
+        p.delta_t[base] = acc;
+      } else if (il == 0) {
+        atomicCAS(p.err, 0, kErrSeqTooLong);
+      }
+    }
+    // the last row of a sequence fills the padding rows of its final stat tile
+    if (ok && il == len - 1 && (len % kStatTile) != 0) {
+      const size_t base = stat_index(p, h, s, il / kStatTile);
+      for (int pr = (len % kStatTile) + sub; pr < kStatTile; pr += 8) {
+        p.lse2[base + pr] = __int_as_float(0x7f800000);  // +inf: exp2(x - inf) = 0
+        p.delta_t[base + pr] = 0.f;
+      }
+    }
+    if (zero_dq) {
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + r * p.Dqk);
+      for (int c = sub; c < p.Dqk / 4; c += 8) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (zero_dkdv && h < p.Hkv) {
+      const long long rk = (static_cast<long long>(b) * p.Hkv + h) * p.S + i;
+      float4* zk = reinterpret_cast<float4*>(p.dk_acc + rk * p.Dqk);
+      for (int c = sub; c < p.Dqk / 4; c += 8) zk[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4* zv = reinterpret_cast<float4*>(p.dv_acc + rk * p.Dv);
+      for (int c = sub; c < p.Dv / 4; c += 8) zv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// out[e] = dtype(acc[e] * mul), 8 elements per thread-iteration.
+template <typename T>
+__global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ acc, T* __restrict__ out, long long n,
+                                                   float mul) {
+  const long long n8 = n / 8;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * e);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * e + 1);
+    uint4 r;
+    constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+    r.x = pack2<BF>(a.x * mul, a.y * mul);
+    r.y = pack2<BF>(a.z * mul, a.w * mul);
+    r.z = pack2<BF>(b.x * mul, b.y * mul);
+    r.w = pack2<BF>(b.z * mul, b.w * mul);
+    reinterpret_cast<uint4*>(out)[e] = r;
+  }
+}
+
+// One block per head; fixed-order reduction (deterministic).
+__global__ void __launch_bounds__(512) dsink_kernel(int B, int Hq, int S, const float* __restrict__ sink,
+                                                    const float* __restrict__ lse,
+                                                    const float* __restrict__ delta, float* __restrict__ dsink) {
+  const int h = blockIdx.x;
+  const float sh = __ldg(sink + h);
+  float acc = 0.f;
+  for (int b = 0; b < B; ++b) {
+    const size_t base = (static_cast<size_t>(b) * Hq + h) * S;
+    for (int i = threadIdx.x; i < S; i += blockDim.x) acc += __expf(sh - __ldg(lse + base + i)) * __ldg(delta + base + i);
+  }
+  __shared__ float red[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) dsink[h] = -v;
+  }
+}
+
+// Waits on a barrier that nothing completes: exercises the timeout path.
+__global__ void selftest_wait_kernel(int* err, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitGuard g{err, &abort_flag, limit};
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, g, 0x7e);
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_preprocess(const Problem& p, int dtype_bf16, const void* o, const void* dout, const float* lse,
+                              float* delta, bool zero_dq, bool zero_dkdv, int num_sms, cudaStream_t st) {
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.S;
+  long long blocks = (rows + 31) / 32;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+#define GQA_PRE(T, DV)                                                                                \
+  preprocess_kernel<T, DV><<<static_cast<unsigned>(blocks), 256, 0, st>>>(                            \
+      p, static_cast<const T*>(o), static_cast<const T*>(dout), lse, delta, zero_dq, zero_dkdv)
+  if (dtype_bf16) {
+    if (p.Dv == 64) GQA_PRE(__nv_bfloat16, 64);
+    else GQA_PRE(__nv_bfloat16, 128);
+  } else {
+    if (p.Dv == 64) GQA_PRE(__half, 64);
+    else GQA_PRE(__half, 128);
+  }
+#undef GQA_PRE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast(const float* acc, void* out, long long n, float mul, int dtype_bf16, int num_sms,
+                        cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  long long blocks = (n / 8 + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (dtype_bf16)
+    cast_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        acc, static_cast<__nv_bfloat16*>(out), n, mul);
+  else
+    cast_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, static_cast<__half*>(out), n, mul);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dsink(int B, int Hq, int S, const float* sink, const float* lse, const float* delta,
+                         float* dsink, cudaStream_t st) {
+  dsink_kernel<<<Hq, 512, 0, st>>>(B, Hq, S, sink, lse, delta, dsink);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(int* err, long long limit, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(err, limit);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

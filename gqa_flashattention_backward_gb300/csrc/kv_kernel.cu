@@ -1,0 +1,526 @@
+// Key/value-stationary tcgen05 backward main kernel.
+//
+// One CTA owns 128 key/value rows (one KV tile) of one kv head and streams the
+// query tiles that can see them (tilelang PR #1093 "[GQA] Add regional atomic
+// add", Additional comments: per-KV-block CTAs, a k_base loop over query blocks,
+// dQ added per iteration, dK/dV accumulated locally and added once into kv head
+// "bx // groups").  Per query tile it computes (tilelang-ascend PR #1638 "Add GQA
+// Sink Backward BHSD", review thread k1..k5), transposed so the 128 key rows
+// sit on the 128 TMEM lanes:
+//
+//   S^T  = K . Q^T                (tcgen05, fp32 in TMEM)
+//   P^T  = exp2(S^T*scale*log2e - LSE2_i), masked      (CUDA cores, packed to 16-bit in TMEM)
+//   dP^T = V . dO^T               (tcgen05)
+//   dS^T = P^T * (dP^T - Delta_i) (CUDA cores; 16-bit in TMEM and, for dQ, in shared memory)
+//   dV  += P^T . dO               (tcgen05, A operand from TMEM)
+//   dK  += dS^T . Q               (tcgen05, A operand from TMEM)
+//   dQ_partial = dS . K           (tcgen05) -> added into an fp32 dQ accumulator
+//
+// The softmax scale is left out of dS and applied once to dK (epilogue) and dQ
+// (postprocess).  Group reduction of dK/dV over the Hq/Hkv query heads:
+//   group_tmem = 1 : the CTA loops over every query head of its kv head, so dK/dV
+//                    stay in TMEM and are written once as fp16/bf16 (no atomics);
+//   group_tmem = 0 : one CTA per query head; after its loop it adds dK/dV into
+//                    fp32 accumulators (red.v4 / bulk tensor reduce / scalar red).
+// dQ partials are added with red.global.add.v4.f32, a bulk tensor reduce from
+// shared memory (cp.reduce.async.bulk.tensor), or per-element red.f32 (triton
+// issue #4717 "atomic_add slows down attention backwards due to layout
+// conversions": vectorised atomics against scalar ones).
+//
+// Warp roles (320 threads): warps 0-3 softmax/dS warpgroup (thread r = key row r
+// = TMEM lane r); warps 4-7 dQ drain warpgroup (thread r = query row r); warp 8
+// TMA producer; warp 9 TMEM allocator + MMA issuer.
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <type_traits>
+#include "common.cuh"
+#include "umma.cuh"
+#include "launch.h"
+
+namespace gqa {
+
+template <int DQK, int DV>
+struct KvCfg {
+  static constexpr int BK = 128;
+  static constexpr int BQ = (DQK == 192) ? 64 : 128;
+  static constexpr bool HAS_DQ = (DQK != 192);          // (192,128): dQ from the query-stationary pass
+  static constexpr bool DQ_ALIAS = (DQK == 128);         // dQ accumulator shares the dP/dS columns
+  static constexpr bool HAS_STAGING = (DQK == 64);       // shared staging for the bulk dQ reduce
+  static constexpr int K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
+  static constexpr int Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
+  static constexpr int ST = (DQK == 64) ? 3 : ((DQK == 128) ? 2 : 3);
+  static constexpr int DS_BYTES = HAS_DQ ? BQ * BK * 2 : 0;
+  static constexpr int STG_BYTES = HAS_STAGING ? 4 * 2 * 32 * 32 * 4 : 0;
+  // shared-memory map (offsets from a 1024-aligned base)
+  static constexpr int OFF_K = 0, OFF_V = OFF_K + K_BYTES;
+  static constexpr int OFF_Q = OFF_V + V_BYTES;                  // stage st at OFF_Q + st*Q_BYTES
+  static constexpr int OFF_DO = OFF_Q + ST * Q_BYTES;
+  static constexpr int OFF_DS = OFF_DO + ST * DO_BYTES;
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;
+  static constexpr int OFF_LSE = OFF_STG + STG_BYTES;           // ST x BQ floats
+  static constexpr int OFF_DEL = OFF_LSE + ST * BQ * 4;
+  static constexpr int OFF_CTL = OFF_DEL + ST * BQ * 4;
+  static constexpr int SMEM = OFF_CTL + 256;
+  // TMEM columns
+  static constexpr uint32_t T_S = 0, T_DP = BQ, T_DV = 2 * BQ, T_DK = 2 * BQ + DV;
+  static constexpr uint32_t T_DQ = DQ_ALIAS ? T_DP : (T_DK + DQK);
+  static constexpr int THREADS = 320;
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(T_DK + DQK <= 512 && (!HAS_DQ || DQ_ALIAS || T_DQ + DQK <= 512), "tmem");
+};
+
+struct KvCtl {
+  uint64_t kv_full;
+  uint64_t q_full[3], do_full[3], q_empty[3];
+  uint64_t s_full, dp_full, p_full, ds_full;
+  uint64_t dq_full, dq_empty, dsmem_free, acc_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(KvCtl) <= 256, "ctl");
+
+__device__ __forceinline__ bool kv_allowed(int i, int j, int len, int causal, int window) {
+  return j < len && (!causal || j <= i) && (window <= 0 || i - j < window);
+}
+
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Adds a warp's 32 rows x 32 fp32 columns (one row per lane, in v[]) into a
+// global fp32 accumulator, by the chosen mode.  `grow` = global row of this lane
+// (row of [rows][ld]), `valid` = lane's row is inside its sequence.
+template <int MODE>
+__device__ __forceinline__ void add_row32(float* acc, size_t grow, int ld, int c0, const uint32_t (&v)[32],
+                                          bool valid) {
+  if (!valid) return;
+  float* dst = acc + grow * ld + c0;
+  if (MODE == kDqRedV4) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      red_add_v4(dst + 4 * q, __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+  } else if (MODE == kDqScalar) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) red_add_f32(dst + e, __uint_as_float(v[e]));
+  } else if (MODE == kDqStore) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+  }
+}
+
+// Bulk path: stage a warp's 32x32 fp32 block in 128B-swizzled shared memory
+// (the layout the fp32 reduce tensor map expects) and reduce it with one TMA op.
+__device__ __forceinline__ void stage_and_reduce(uint8_t* stg, const CUtensorMap* map, int lane, const uint32_t (&v)[32],
+                                                 int x, int y, int z) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t off = lane * 128 + ((q ^ (lane & 7)) * 16);
+    *reinterpret_cast<uint4*>(stg + off) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_reduce_add_3d(map, stg, x, y, z);
+    bulk_commit();
+  }
+}
+
+template <int DQK, int DV, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    kv_kernel(const Problem p, const __grid_constant__ Maps m, const int group_tmem, const int dq_mode,
+              const int kv_mode, void* __restrict__ dk_out, void* __restrict__ dv_out) {
+  using C = KvCfg<DQK, DV>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  KvCtl& ctl = *reinterpret_cast<KvCtl*>(smem + C::OFF_CTL);
+
+  const int head = blockIdx.x;   // kv head (group_tmem) or query head
+  const int s = blockIdx.z;
+  Seq sq;
+  if (!load_seq(p, s, sq)) return;
+  const int ntk = (sq.len + C::BK - 1) / C::BK;
+  const int kt = blockIdx.y;     // tile 0 has the most query tiles under a causal mask: launched first
+  if (kt >= ntk) return;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the operand layout needs a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, 0x40000010);
+    return;
+  }
+  int t0, t1;
+  q_tiles_for_kv_tile(kt, sq.len, C::BQ, p.causal, p.window, &t0, &t1);
+  const int nt = t1 - t0;
+  const int g = group_tmem ? head : head / p.G;
+  const int nh = group_tmem ? p.G : 1;
+  const int h_first = group_tmem ? g * p.G : head;
+  const int NIT = nh * nt;
+  const int j0 = kt * C::BK;
+  const int zk = sq.b * p.Hkv + g;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&ctl.kv_full, 1);
+    for (int i = 0; i < C::ST; ++i) {
+      mbar_init(&ctl.q_full[i], 1);
+      mbar_init(&ctl.do_full[i], 1);
+      mbar_init(&ctl.q_empty[i], 1);
+    }
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.dp_full, 1);
+    mbar_init(&ctl.p_full, 128);
+    mbar_init(&ctl.ds_full, 128);
+    mbar_init(&ctl.dq_full, 1);
+    mbar_init(&ctl.dq_empty, 128);
+    mbar_init(&ctl.dsmem_free, 1);
+    mbar_init(&ctl.acc_done, 1);
+    ctl.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&ctl.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const WaitGuard guard{p.err, &ctl.abort_flag, p.wait_limit};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&m.q);
+      tma_prefetch_map(&m.dout);
+      mbar_expect_tx(&ctl.kv_full, C::K_BYTES + C::V_BYTES);
+      const int krow = sq.start + j0;
+      for (int cb = 0; cb < DQK / 64; ++cb)
+        tma_load_3d(smem + C::OFF_K + cb * (C::BK * 128), &m.k, &ctl.kv_full, cb * 64, krow, zk);
+      for (int cb = 0; cb < DV / 64; ++cb)
+        tma_load_3d(smem + C::OFF_V + cb * (C::BK * 128), &m.v, &ctl.kv_full, cb * 64, krow, zk);
+      int issued = 0;
+      for (int it = 0; it < NIT; ++it) {
+        const int st = it % C::ST;
+        if (it >= C::ST && !mbar_wait(&ctl.q_empty[st], ((it / C::ST) - 1) & 1, guard, 11)) break;
+        const int h = h_first + it / nt;
+        const int t = t0 + it % nt;
+        const int zq = sq.b * p.Hq + h;
+        const int qrow = sq.start + t * C::BQ;
+        uint8_t* sQ = smem + C::OFF_Q + st * C::Q_BYTES;
+        uint8_t* sDO = smem + C::OFF_DO + st * C::DO_BYTES;
+        float* sL = reinterpret_cast<float*>(smem + C::OFF_LSE) + st * C::BQ;
+        float* sD = reinterpret_cast<float*>(smem + C::OFF_DEL) + st * C::BQ;
+        const size_t sidx = stat_index(p, h, s, (t * C::BQ) / kStatTile) + (t * C::BQ) % kStatTile;
+        mbar_expect_tx(&ctl.q_full[st], C::Q_BYTES + 2 * C::BQ * 4);
+        for (int cb = 0; cb < DQK / 64; ++cb)
+          tma_load_3d(sQ + cb * (C::BQ * 128), &m.q, &ctl.q_full[st], cb * 64, qrow, zq);
+        bulk_load(sL, p.lse2 + sidx, C::BQ * 4, &ctl.q_full[st]);
+        bulk_load(sD, p.delta_t + sidx, C::BQ * 4, &ctl.q_full[st]);
+        mbar_expect_tx(&ctl.do_full[st], C::DO_BYTES);
+        for (int cb = 0; cb < DV / 64; ++cb)
+          tma_load_3d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.do_full[st], cb * 64, qrow, zq);
+        issued = it + 1;
+      }
+      if (ctl.abort_flag) {
+        volatile int no_abort = 0;
+        const WaitGuard g2{nullptr, &no_abort, p.wait_limit};
+        mbar_wait(&ctl.kv_full, 0, g2, 0);
+        for (int it = issued - C::ST < 0 ? 0 : issued - C::ST; it < issued; ++it) {
+          mbar_wait(&ctl.q_full[it % C::ST], (it / C::ST) & 1, g2, 0);
+          mbar_wait(&ctl.do_full[it % C::ST], (it / C::ST) & 1, g2, 0);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_f16(128, C::BQ, BF16, false, false);
+      constexpr uint32_t idDV = idesc_f16(128, DV, BF16, false, true);
+      constexpr uint32_t idDK = idesc_f16(128, DQK, BF16, false, true);
+      constexpr uint32_t idDQ = idesc_f16(C::BQ, DQK, BF16, true, true);
+      const uint32_t aK = smem_u32(smem + C::OFF_K), aV = smem_u32(smem + C::OFF_V);
+      const uint32_t aDS = smem_u32(smem + C::OFF_DS);
+      const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
+      bool ok = mbar_wait(&ctl.kv_full, 0, guard, 12);
+      auto issue_s = [&](int it) -> bool {
+        const int st = it % C::ST;
+        if (!mbar_wait(&ctl.q_full[st], (it / C::ST) & 1, guard, 13)) return false;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(smem + C::OFF_Q + st * C::Q_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          umma_ss(tmem + C::T_S, sdesc_sw128(aK + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024),
+                  sdesc_sw128(aQ + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+        umma_commit(&ctl.s_full);
+        return true;
+      };
+      auto issue_dp = [&](int it) -> bool {
+        const int st = it % C::ST;
+        if (!mbar_wait(&ctl.do_full[st], (it / C::ST) & 1, guard, 14)) return false;
+        // the dQ accumulator shares these columns: its drain must be finished
+        if (C::DQ_ALIAS && dq_on && it >= 1 && !mbar_wait(&ctl.dq_empty, (it - 1) & 1, guard, 15)) return false;
+        tc_fence_after();
+        const uint32_t aDO = smem_u32(smem + C::OFF_DO + st * C::DO_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk)
+          umma_ss(tmem + C::T_DP, sdesc_sw128(aV + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024),
+                  sdesc_sw128(aDO + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+        umma_commit(&ctl.dp_full);
+        return true;
+      };
+      if (ok && NIT > 0) ok = issue_s(0) && issue_dp(0);
+      for (int it = 0; ok && it < NIT; ++it) {
+        const int st = it % C::ST;
+        const uint32_t aQ = smem_u32(smem + C::OFF_Q + st * C::Q_BYTES);
+        const uint32_t aDO = smem_u32(smem + C::OFF_DO + st * C::DO_BYTES);
+        // dV += P^T . dO
+        if (!mbar_wait(&ctl.p_full, it & 1, guard, 16)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          umma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, sdesc_sw128(aDO + kk * 2048, C::BQ * 128, 1024), idDV,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        // next tile's S^T (its columns were read by the softmax warps, P^T was consumed by the dV MMA above)
+        if (it + 1 < NIT && !issue_s(it + 1)) break;
+        // dK += dS^T . Q
+        if (!mbar_wait(&ctl.ds_full, it & 1, guard, 17)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          umma_ts(tmem + C::T_DK, tmem + C::T_DP + kk * 8, sdesc_sw128(aQ + kk * 2048, C::BQ * 128, 1024), idDK,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        // dQ_partial = dS . K
+        if (dq_on) {
+          if (!C::DQ_ALIAS && it >= 1 && !mbar_wait(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk)
+            umma_ss(tmem + C::T_DQ, sdesc_sw128(aDS + kk * 2048, C::BK * 128, 1024),
+                    sdesc_sw128(aK + kk * 2048, C::BK * 128, 1024), idDQ, kk > 0);
+          umma_commit(&ctl.dq_full);
+          umma_commit(&ctl.dsmem_free);
+        }
+        umma_commit(&ctl.q_empty[st]);
+        if (it + 1 < NIT && !issue_dp(it + 1)) break;
+      }
+      umma_commit(&ctl.acc_done);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ dQ drain warpgroup
+    if (C::HAS_DQ && dq_mode != kDqNone) {
+      const int r = tid - 128;  // query row within the tile == TMEM lane
+      const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+      uint8_t* stg = smem + C::OFF_STG + (warp - 4) * (2 * 32 * 32 * 4);
+      int nbulk = 0;
+      for (int it = 0; it < NIT; ++it) {
+        const int h = h_first + it / nt;
+        const int t = t0 + it % nt;
+        const int il = t * C::BQ + r;
+        if (!mbar_wait_warp(&ctl.dq_full, it & 1, guard, 19)) break;
+        tc_fence_after();
+        uint32_t v[DQK / 32][32];
+#pragma unroll
+        for (int c = 0; c < DQK / 32; ++c) tmem_ld32(tmem + lane_base + C::T_DQ + 32 * c, v[c]);
+        tc_fence_before();
+        mbar_arrive(&ctl.dq_empty);
+        const size_t grow = (static_cast<size_t>(sq.b) * p.Hq + h) * p.S + sq.start + il;
+        const bool valid = il < sq.len;
+#pragma unroll
+        for (int c = 0; c < DQK / 32; ++c) {
+          const int c0 = 32 * c;
+          const uint32_t(&vc)[32] = v[c];
+          if (dq_mode == kDqRedV4) add_row32<kDqRedV4>(p.dq_acc, grow, DQK, c0, vc, valid);
+          else if (dq_mode == kDqScalar) add_row32<kDqScalar>(p.dq_acc, grow, DQK, c0, vc, valid);
+          else if (dq_mode == kDqStore) add_row32<kDqStore>(p.dq_acc, grow, DQK, c0, vc, valid);
+          else if (C::HAS_STAGING) {
+            uint8_t* buf = stg + (nbulk & 1) * (32 * 32 * 4);
+            if (lane == 0 && nbulk >= 1) bulk_wait_read1();
+            __syncwarp();
+            stage_and_reduce(buf, &m.dq_acc, lane, vc, c0, sq.start + t * C::BQ + (warp - 4) * 32,
+                             sq.b * p.Hq + h);
+            ++nbulk;
+          }
+        }
+      }
+      if (lane == 0 && nbulk > 0) bulk_wait0();
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / dS warpgroup
+    const int r = tid;                 // key row within the tile == TMEM lane
+    const int j = j0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
+    bool ok = true;
+    for (int it = 0; it < NIT; ++it) {
+      const int st = it % C::ST;
+      const int t = t0 + it % nt;
+      const int i0 = t * C::BQ;
+      const bool need_mask = (j0 + C::BK > sq.len) || (p.causal && i0 < j0 + C::BK - 1) ||
+                             (p.window > 0 && i0 + C::BQ - 1 - j0 >= p.window);
+      const float* sL = reinterpret_cast<const float*>(smem + C::OFF_LSE) + st * C::BQ;
+      const float* sD = reinterpret_cast<const float*>(smem + C::OFF_DEL) + st * C::BQ;
+      if (!mbar_wait_warp(&ctl.q_full[st], (it / C::ST) & 1, guard, 20) ||
+          !mbar_wait_warp(&ctl.s_full, it & 1, guard, 21)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // P^T = exp2(S^T * scale*log2e - LSE2), kept packed in registers for dS
+      uint32_t pk[C::BQ / 2];
+#pragma unroll
+      for (int c0 = 0; c0 < C::BQ; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::T_S + c0, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float a = ex2_approx(fmaf(__uint_as_float(v[2 * e]), sl2, -sL[c0 + 2 * e]));
+          float b = ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -sL[c0 + 2 * e + 1]));
+          if (need_mask) {
+            if (!kv_allowed(i0 + c0 + 2 * e, j, sq.len, p.causal, p.window)) a = 0.f;
+            if (!kv_allowed(i0 + c0 + 2 * e + 1, j, sq.len, p.causal, p.window)) b = 0.f;
+          }
+          pk[c0 / 2 + e] = pack2<BF16>(a, b);
+        }
+        uint32_t pc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pc[e] = pk[c0 / 2 + e];
+        tmem_st16(tmem + lane_base + C::T_S + c0 / 2, pc);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctl.p_full);
+      // dS^T = P^T * (dP^T - Delta)
+      if (!mbar_wait_warp(&ctl.dp_full, it & 1, guard, 22)) {
+        ok = false;
+        break;
+      }
+      if (dq_on && it >= 1 && !mbar_wait_warp(&ctl.dsmem_free, (it - 1) & 1, guard, 23)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < C::BQ; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::T_DP + c0, v);
+        uint32_t ds[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float2 pp;
+          if (BF16) pp = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c0 / 2 + e]));
+          else pp = __half22float2(*reinterpret_cast<const __half2*>(&pk[c0 / 2 + e]));
+          const float a = pp.x * (__uint_as_float(v[2 * e]) - sD[c0 + 2 * e]);
+          const float b = pp.y * (__uint_as_float(v[2 * e + 1]) - sD[c0 + 2 * e + 1]);
+          ds[e] = pack2<BF16>(a, b);
+        }
+        tmem_st16(tmem + lane_base + C::T_DP + c0 / 2, ds);
+        if (dq_on) {
+          // dS for the dQ MMA: MN-major (query index contiguous), 128B swizzle, key row r = K index
+          uint8_t* sds = smem + C::OFF_DS + (c0 / 64) * (C::BK * 128) + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = ((c0 % 64) / 8 + q) ^ (r & 7);
+            *reinterpret_cast<uint4*>(sds + chunk * 16) = make_uint4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]);
+          }
+        }
+      }
+      tmem_st_wait();
+      if (dq_on) fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&ctl.ds_full);
+    }
+    // ---------------------------------------------------------- dK / dV epilogue
+    if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 24)) {
+      tc_fence_after();
+      const bool valid = j < sq.len;
+      const size_t krow = static_cast<size_t>(zk) * p.S + sq.start + j;
+      uint8_t* stg = smem + C::OFF_Q + warp * (2 * 32 * 32 * 4);  // stage buffers are idle now
+      int nbulk = 0;
+      auto emit = [&](uint32_t tcol, int D, void* out, float* acc, const CUtensorMap* map, float mul) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[32];
+          if (NIT > 0) tmem_ld32(tmem + lane_base + tcol + c0, v);
+          else
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          if (group_tmem) {
+            if (valid) {
+              T* o = static_cast<T*>(out) + krow * D + c0;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 w;
+                w.x = pack2<BF16>(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul);
+                w.y = pack2<BF16>(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul);
+                w.z = pack2<BF16>(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul);
+                w.w = pack2<BF16>(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul);
+                *reinterpret_cast<uint4*>(o + 8 * q) = w;
+              }
+            }
+          } else if (kv_mode == kDqRedV4) {
+            add_row32<kDqRedV4>(acc, krow, D, c0, v, valid);
+          } else if (kv_mode == kDqScalar) {
+            add_row32<kDqScalar>(acc, krow, D, c0, v, valid);
+          } else if (kv_mode == kDqStore) {
+            add_row32<kDqStore>(acc, krow, D, c0, v, valid);
+          } else {
+            uint8_t* buf = stg + (nbulk & 1) * (32 * 32 * 4);
+            if (lane == 0 && nbulk >= 1) bulk_wait_read1();
+            __syncwarp();
+            stage_and_reduce(buf, map, lane, v, c0, sq.start + j0 + warp * 32, zk);
+            ++nbulk;
+          }
+        }
+      };
+      emit(C::T_DV, DV, dv_out, p.dv_acc, &m.dv_acc, 1.f);
+      emit(C::T_DK, DQK, dk_out, p.dk_acc, &m.dk_acc, p.scale);
+      if (lane == 0 && nbulk > 0) bulk_wait0();
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV, bool BF16>
+static cudaError_t launch_kv_t(const Problem& p, const Maps& m, const KvLaunch& kl, cudaStream_t st) {
+  using C = KvCfg<DQK, DV>;
+  auto kern = kv_kernel<DQK, DV, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int ntk = (p.max_len + C::BK - 1) / C::BK;
+  if (ntk == 0 || p.nseqs == 0) return cudaSuccess;
+  dim3 grid(kl.group_tmem ? p.Hkv : p.Hq, ntk, p.nseqs);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(p, m, kl.group_tmem, C::HAS_DQ ? kl.dq_mode : kDqNone, kl.kv_red_mode,
+                                          kl.dk, kl.dv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_kv(const Problem& p, int dtype_bf16, const Maps& m, const KvLaunch& kl, cudaStream_t st) {
+#define GQA_KV(DQK, DV)                                                                            \
+  if (p.Dqk == DQK && p.Dv == DV)                                                                  \
+    return dtype_bf16 ? launch_kv_t<DQK, DV, true>(p, m, kl, st) : launch_kv_t<DQK, DV, false>(p, m, kl, st);
+  GQA_KV(64, 64)
+  GQA_KV(128, 128)
+  GQA_KV(192, 128)
+#undef GQA_KV
+  return cudaErrorInvalidValue;
+}
+
+bool kv_kernel_has_dq(int Dqk) { return Dqk != 192; }
+bool kv_kernel_has_bulk_dq(int Dqk) { return Dqk == 64; }
+int kv_kernel_bq(int Dqk) { return Dqk == 192 ? 64 : 128; }
+
+}  // namespace gqa
