@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Benchmark of the GQA FlashAttention backward on GB300.
+
+One step = the whole backward hot path on one batch of synthetic input that is
+already resident in HBM: gqa_attn_bwd_preprocess (Delta, row statistics,
+accumulator zeroing) -> gqa_attn_bwd (main kernel) -> gqa_attn_bwd_postprocess
+(fp32 -> fp16 casts) [-> gqa_attn_dsink when the workload has a sink].  The
+forward that produces O and LSE runs once, untimed.
+
+Workload: the causal MHA backward B=4, H=8, d=64, fp16 (the Triton
+fused-attention table's shape), headline N_CTX=16384, plus a sweep over
+N_CTX in {2048..32768}.  TFLOPS use the 2.5 x forward, causal-halved count.
+
+The inputs of a step (Q,K,V,O,dO plus the fp32 dQ accumulator) are larger than
+the 129 MB L2, so steps run back to back with no flush in between.
+
+`--impl reference` times the fp64 CPU oracle instead (bounded sample).
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path has no data exchange); value = all ranks' FLOPs / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE_N = 16384
+SWEEP = (2048, 4096, 8192, 16384, 32768)
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"])
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), reasons=sorted(reasons), samples=len(sm))
+
+
+def _src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gqa_flashattention_backward_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_key: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_sha") == src_hash:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import gqa_flashattention_backward_gb300 as pkg
+    from gqa_flashattention_backward_gb300 import _native as nat
+    from gqa_flashattention_backward_gb300 import workloads as W
+
+    ws_n, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if ws_n > 1:
+            dist.barrier()
+
+    nat.load()
+    peaks = _peaks()
+
+    def setup(w, red_mode=nat.GQA_RED_V4, group_mode=nat.GQA_GROUP_TMEM, deterministic=False):
+        q, k, v, do, sink = W.make_inputs(w)
+        q, k, v, do = (t.to(dev) for t in (q, k, v, do))
+        sink = sink.to(dev) if sink is not None else None
+        cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev) if w.cu_seqlens else None
+        kw = dict(causal=w.causal, window=w.window, scale=w.resolved_scale, cu_seqlens=cu,
+                  max_seqlen=w.max_seqlen if cu is not None else None)
+        o, lse = pkg.attention_forward(q, k, v, sink=sink, **kw)
+        p = pkg._params(q, k, v, w.causal, w.window, w.resolved_scale, cu, kw["max_seqlen"], group_mode, red_mode,
+                        deterministic)
+        wsb = nat.alloc_workspace(p, dev)
+        out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                   delta=torch.empty(lse.shape, dtype=torch.float32, device=dev))
+        if sink is not None:
+            out["dsink"] = torch.empty(w.Hq, dtype=torch.float32, device=dev)
+        return dict(w=w, q=q, k=k, v=v, do=do, o=o, lse=lse, sink=sink, p=p, ws=wsb, out=out)
+
+    def step(c, ev=None):
+        """One backward pass through the C ABI; returns the number of kernels launched."""
+        p, o = c["p"], c["out"]
+        nat.bwd_preprocess(p, c["o"], c["do"], c["lse"], o["delta"], c["ws"])
+        if ev is not None:
+            ev[0].record()
+        nat.bwd(p, c["q"], c["k"], c["v"], c["do"], o["dq"], o["dk"], o["dv"], c["ws"])
+        if ev is not None:
+            ev[1].record()
+        nat.bwd_postprocess(p, o["dq"], o["dk"], o["dv"], c["ws"])
+        n = 3
+        if c["sink"] is not None:
+            nat.dsink(p, c["sink"], c["lse"], o["delta"], o["dsink"])
+            n += 1
+        return n
+
+    def timed(c, steps, warmup, main_events=False):
+        for _ in range(warmup):
+            step(c)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)] \
+            if main_events else [None] * steps
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        launches = 0
+        t0.record()
+        for i in range(steps):
+            launches += step(c, evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+        barrier()
+        ms = t0.elapsed_time(t1)
+        main_ms = sum(a.elapsed_time(b) for a, b in evs) / steps if main_events else None
+        return ms, main_ms, launches
+
+    def max_over_ranks(x):
+        if ws_n == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    w = W.mha_causal(args.n_ctx)
+    c = setup(w)
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms, main_ms, launches = timed(c, args.steps, args.warmup, main_events=True)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(total_ms)
+    ms_step = total_ms / args.steps
+    flops_conv = w.flops_convention()
+    flops_exact = w.flops_exact()
+    value = ws_n * flops_conv / (ms_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (the backward main kernel)
+    achieved = flops_exact / (main_ms * 1e-3) / 1e12
+    src = _src_hash("kv_kernel.cu", "umma.cuh", "common.cuh")
+    traffic = _traffic(f"kv_kernel/{w.name}", src)
+    roofline = dict(bound="tensor", achieved=round(achieved, 2), peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=round(achieved / peaks["bf16_tflops"], 4), traffic=traffic,
+                    kernel="kv_kernel<64,64,fp16>", kernel_ms=round(main_ms, 4),
+                    flops_per_launch=flops_exact, peak_source=f"{peaks['source']} bf16 burst (fp16 same rate)")
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = {n: c[n].cpu().pin_memory() for n in ("q", "k", "v", "o", "do", "lse")}
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        host_out = {n: torch.empty(c["out"][n].shape, dtype=c["out"][n].dtype).pin_memory() for n in ("dq", "dk", "dv")}
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        dbuf = {n: torch.empty_like(c[n]) for n in pinned}
+
+        def e2e_step():
+            for n, t in pinned.items():
+                dbuf[n].copy_(t, non_blocking=True)
+            r = pkg.attention_backward(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["o"], dbuf["lse"], dbuf["do"],
+                                       causal=w.causal, scale=w.resolved_scale, workspace=c["ws"], out=c["out"])
+            for n in ("dq", "dk", "dv"):
+                host_out[n].copy_(r[n], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        t1.record()
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = max_over_ranks(t0.elapsed_time(t1)) / args.steps
+        e2e = dict(value=round(ws_n * flops_conv / (e_ms * 1e-3) / 1e12, 2), unit="TFLOPS", ms_per_step=round(e_ms, 3),
+                   h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h)
+        del pinned, host_out, dbuf
+
+    # accumulation variants at the headline size (p3's atomic_add / none comparison)
+    variants = {}
+    if not args.no_variants:
+        for name, kw in (("tmem_red_v4", dict()), ("tmem_red_none", dict(red_mode=nat.GQA_RED_NONE)),
+                         ("tmem_red_bulk", dict(red_mode=nat.GQA_RED_BULK)),
+                         ("tmem_red_scalar", dict(red_mode=nat.GQA_RED_SCALAR)),
+                         ("atomic_red_v4", dict(group_mode=nat.GQA_GROUP_ATOMIC)),
+                         ("deterministic", dict(deterministic=True))):
+            cv = setup(w, **kw)
+            ms, mms, _ = timed(cv, max(3, args.steps // 2), args.warmup, main_events=True)
+            variants[name] = dict(tflops=round(flops_conv / (ms / max(3, args.steps // 2) * 1e-3) / 1e12, 2),
+                                  main_kernel_ms=round(mms, 4))
+            del cv
+        if "tmem_red_none" in variants:
+            variants["accumulation_overhead_vs_none"] = round(
+                variants["tmem_red_none"]["tflops"] / variants["tmem_red_v4"]["tflops"] - 1.0, 4)
+
+    sweep = {}
+    if not args.no_sweep:
+        for n in SWEEP:
+            ws_ = W.mha_causal(n)
+            cs = setup(ws_)
+            ms, mms, _ = timed(cs, max(3, args.steps // 2), args.warmup, main_events=True)
+            stp = ms / max(3, args.steps // 2)
+            sweep[str(n)] = dict(tflops=round(ws_.flops_convention() / (stp * 1e-3) / 1e12, 2),
+                                 ms=round(stp, 4), main_kernel_tflops_exact=round(
+                                     ws_.flops_exact() / (mms * 1e-3) / 1e12, 2))
+            del cs
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if ws_n == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(args)
+        line = dict(metric="GQA attention bwd TFLOPS (1xGB300, causal)", value=round(value, 2), unit="TFLOPS",
+                    n_gpus=ws_n, steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 4),
+                    higher_is_better=True, scaling="weak", vs_baseline=None, dtype="fp16", data="synthetic",
+                    config=dict(workload=w.name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, S=w.S, D=w.Dqk, causal=True,
+                                flop_count="2.5x forward, causal-halved", l2="inputs larger than L2, no flush",
+                                parallelism=f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
+                                mode="group_tmem + red.v4 dQ"),
+                    flops_per_step_convention=flops_conv, flops_per_step_exact=flops_exact,
+                    frac_of_peak_exact=round(flops_exact / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                    roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clocks,
+                    variants=variants, sweep=sweep)
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
+def _oracle_sample(n: int):
+    """(workload, timer) for the oracle backward of one (batch, head) of the causal
+    d=64 workload at length n; timer() runs it once and returns seconds."""
+    from gqa_flashattention_backward_gb300 import workloads as W
+    from oracle import oracle as orc
+
+    w = W.shrink(W.mha_causal(n), name=f"oracle_sample_n{n}", B=1, Hq=1, Hkv=1)
+    q, k, v, do, _ = W.make_inputs(w)
+    f = lambda t: t.double().numpy()  # noqa: E731
+    q, k, v, do = f(q), f(k), f(v), f(do)
+    pb = orc.Problem(B=1, Hq=1, Hkv=1, S=n, Dqk=64, Dv=64, causal=True, scale=w.resolved_scale)
+    o, lse = orc.forward(pb, q, k, v)
+
+    def timer():
+        t0 = time.perf_counter()
+        orc.backward(pb, q, k, v, o, lse, do)
+        return time.perf_counter() - t0
+
+    return w, timer
+
+
+def _calibrated_sample(target_s: float):
+    n = 1024
+    while True:
+        w, timer = _oracle_sample(n)
+        dt = timer()
+        if dt * 3.5 > target_s or n >= 16384:
+            return n, w, timer, dt
+        n *= 2
+
+
+def _sample_text(n):
+    return f"fp64 oracle backward of 1 of the 32 (batch, head) pairs at N_CTX={n} (d=64, causal)"
+
+
+def cpu_baseline(args, target_s: float = 12.0):
+    """The oracle timed on the host cores on a bounded sample of the same workload."""
+    n, w, timer, dt = _calibrated_sample(target_s)
+    return dict(value=round(w.flops_convention() / dt / 1e12, 6), unit="TFLOPS",
+                cores=len(os.sched_getaffinity(0)), kind="oracle", seconds=round(dt, 3), sample=_sample_text(n))
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle, each step a bounded sample of the workload."""
+    ws_n, rank, _ = _dist()
+    if rank != 0:
+        return None
+    n, w, timer, _ = _calibrated_sample(1.5)
+    for _ in range(args.warmup):
+        timer()
+    tot = sum(timer() for _ in range(args.steps))
+    val = round(args.steps * w.flops_convention() / tot / 1e12, 6)
+    cores = len(os.sched_getaffinity(0))
+    line = dict(impl="reference", metric="GQA attention bwd TFLOPS (1xGB300, causal)", value=val, unit="TFLOPS",
+                n_gpus=ws_n, steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * tot / args.steps, 3),
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload=f"mha_causal_n{args.n_ctx}", B=4, Hq=8, Hkv=8, S=args.n_ctx, D=64,
+                            causal=True, flop_count="2.5x forward, causal-halved"),
+                cpu_baseline=dict(kind="oracle", cores=cores, sample=_sample_text(n), value=val, unit="TFLOPS"),
+                e2e=dict(value=val, unit="TFLOPS", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--n-ctx", type=int, default=HEADLINE_N)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
