@@ -31,7 +31,7 @@ GQA_RED_V4, GQA_RED_BULK, GQA_RED_SCALAR, GQA_RED_NONE = 0, 1, 2, 3
 EXPORTS = (
     "gqa_attn_workspace_size", "gqa_attn_fwd", "gqa_attn_bwd_preprocess", "gqa_attn_bwd",
     "gqa_attn_bwd_postprocess", "gqa_attn_dsink", "gqa_attn_get_device_error", "gqa_attn_set_wait_limit",
-    "gqa_attn_selftest_wait_timeout", "gqa_attn_strerror",
+    "gqa_attn_selftest_wait_timeout", "gqa_attn_strerror", "gqa_attn_bwd_noalloc",
 )
 
 

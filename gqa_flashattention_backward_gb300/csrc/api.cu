@@ -315,3 +315,50 @@ const char* gqa_attn_strerror(gqa_status s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation backward
+// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is being
+// captured with a relaxed/global capture mode that forbids allocation, allocators
+// that own the whole device pool, and embedded runtimes whose memory is fixed at
+// start-up.  For them gqa_attn_bwd_noalloc runs the backward with its scratch in
+// the file-scope device array below instead of a caller workspace.  The array is
+// part of the library's device image: every GPU that loads the library holds
+// these bytes until the process exits.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once per
+// device; the host-side symbol is only a stand-in and must never reach a kernel).
+gqa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return GQA_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return GQA_OK;
+}
+}  // namespace
+
+extern "C" gqa_status gqa_attn_bwd_noalloc(const gqa_attn_params* p, const void* q, const void* k, const void* v,
+                                           const void* o, const void* dout, const float* lse, float* delta, void* dq,
+                                           void* dk, void* dv, void* stream) {
+  gqa_status s = validate(p);
+  if (s != GQA_OK) return s;
+  if (gqa_attn_workspace_size(p) > kNoAllocScratchBytes) return GQA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != GQA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the error word must start at zero; the other regions are fully rewritten by the preprocess
+  if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return GQA_ERR_CUDA;
+  if ((s = gqa_attn_bwd_preprocess(p, o, dout, lse, delta, scratch, kNoAllocScratchBytes, stream)) != GQA_OK) return s;
+  if ((s = gqa_attn_bwd(p, q, k, v, dout, dq, dk, dv, scratch, kNoAllocScratchBytes, stream)) != GQA_OK) return s;
+  return gqa_attn_bwd_postprocess(p, dq, dk, dv, scratch, kNoAllocScratchBytes, stream);
+}

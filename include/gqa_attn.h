@@ -165,6 +165,26 @@ void gqa_attn_set_wait_limit(long long cycles);
  * the context stays usable.  Needs a workspace of gqa_attn_workspace_size. */
 gqa_status gqa_attn_selftest_wait_timeout(void* workspace, size_t ws_bytes, void* stream);
 
+/* No-allocation backward (no counterpart in the pages: a convenience for callers
+ * that cannot allocate device memory -- e.g. code running inside a CUDA graph
+ * capture that forbids cudaMalloc, or a runtime whose device memory is fixed at
+ * start-up).  Runs gqa_attn_bwd_preprocess, gqa_attn_bwd and
+ * gqa_attn_bwd_postprocess on `stream` with their scratch in a 16 MiB device
+ * array that is part of the library (held on every GPU that loads it until the
+ * process exits) instead of a caller workspace.
+ *   q, k, v, o, dout, lse : inputs as for the three calls above (device).
+ *   delta, dq, dk, dv     : outputs (device), written as by those calls.
+ * Returns GQA_ERR_WORKSPACE when gqa_attn_workspace_size(p) exceeds 16 MiB.
+ * Allocates nothing.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents: calls that overlap on the GPU (other streams, other
+ * threads) race and must be serialised by the caller.  Device-side errors are
+ * recorded in the array and cannot be read back through gqa_attn_get_device_error. */
+gqa_status gqa_attn_bwd_noalloc(const gqa_attn_params* p, const void* q, const void* k, const void* v,
+                                const void* o, const void* dout, const float* lse, float* delta, void* dq,
+                                void* dk, void* dv, void* stream);
+
 /* Human-readable name of a status. */
 const char* gqa_attn_strerror(gqa_status s);
 
