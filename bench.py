@@ -154,7 +154,7 @@ def run_gpu(args):
     nat.load()
     peaks = _peaks()
 
-    def setup(w, red_mode=nat.GQA_RED_V4, group_mode=nat.GQA_GROUP_TMEM, deterministic=False):
+    def setup(w, red_mode=None, group_mode=nat.GQA_GROUP_TMEM, deterministic=False):
         q, k, v, do, sink = W.make_inputs(w)
         q, k, v, do = (t.to(dev) for t in (q, k, v, do))
         sink = sink.to(dev) if sink is not None else None
@@ -271,10 +271,11 @@ def run_gpu(args):
     # accumulation variants at the headline size (p3's atomic_add / none comparison)
     variants = {}
     if not args.no_variants:
-        for name, kw in (("tmem_red_v4", dict()), ("tmem_red_none", dict(red_mode=nat.GQA_RED_NONE)),
+        for name, kw in (("tmem_red_v4", dict(red_mode=nat.GQA_RED_V4)),
+                         ("tmem_red_none", dict(red_mode=nat.GQA_RED_NONE)),
                          ("tmem_red_bulk", dict(red_mode=nat.GQA_RED_BULK)),
                          ("tmem_red_scalar", dict(red_mode=nat.GQA_RED_SCALAR)),
-                         ("atomic_red_v4", dict(group_mode=nat.GQA_GROUP_ATOMIC)),
+                         ("atomic_group_default_red", dict(group_mode=nat.GQA_GROUP_ATOMIC)),
                          ("deterministic", dict(deterministic=True))):
             cv = setup(w, **kw)
             ms, mms, _ = timed(cv, max(3, args.steps // 2), args.warmup, main_events=True)
@@ -282,8 +283,9 @@ def run_gpu(args):
                                   main_kernel_ms=round(mms, 4))
             del cv
         if "tmem_red_none" in variants:
-            variants["accumulation_overhead_vs_none"] = round(
-                variants["tmem_red_none"]["tflops"] / variants["tmem_red_v4"]["tflops"] - 1.0, 4)
+            for v_ in ("tmem_red_v4", "tmem_red_bulk"):
+                variants[f"overhead_{v_}_vs_none"] = round(
+                    variants["tmem_red_none"]["tflops"] / variants[v_]["tflops"] - 1.0, 4)
 
     sweep = {}
     if not args.no_sweep:
@@ -308,7 +310,9 @@ def run_gpu(args):
                     config=dict(workload=w.name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, S=w.S, D=w.Dqk, causal=True,
                                 flop_count="2.5x forward, causal-halved", l2="inputs larger than L2, no flush",
                                 parallelism=f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
-                                mode="group_tmem + red.v4 dQ"),
+                                mode="dK/dV summed in TMEM; dQ by " + (
+                                    "bulk tensor reduce" if pkg.preferred_red_mode(w.Dqk) == nat.GQA_RED_BULK
+                                    else "red.global.add.v4.f32")),
                     flops_per_step_convention=flops_conv, flops_per_step_exact=flops_exact,
                     frac_of_peak_exact=round(flops_exact / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clocks,

@@ -23,14 +23,22 @@ from ._native import (GQA_GROUP_ATOMIC, GQA_GROUP_TMEM, GQA_RED_BULK, GQA_RED_NO
                       GQA_RED_V4, GqaError)
 
 __all__ = [
-    "attention_forward", "attention_backward", "native", "GqaError", "GQA_GROUP_TMEM", "GQA_GROUP_ATOMIC",
+    "attention_forward", "attention_backward", "preferred_red_mode", "native", "GqaError", "GQA_GROUP_TMEM", "GQA_GROUP_ATOMIC",
     "GQA_RED_V4", "GQA_RED_BULK", "GQA_RED_SCALAR", "GQA_RED_NONE",
 ]
 
 
+def preferred_red_mode(Dqk: int) -> int:
+    """The fastest supported dQ reduction: the bulk tensor reduce where the tile has
+    shared-memory staging for it (head dim 64), vectorised red.v4 otherwise."""
+    return GQA_RED_BULK if Dqk == 64 else GQA_RED_V4
+
+
 def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=GQA_GROUP_TMEM,
-            red_mode=GQA_RED_V4, deterministic=False):
+            red_mode=None, deterministic=False):
     B, Hq, S, Dqk = q.shape
+    if red_mode is None:
+        red_mode = preferred_red_mode(Dqk)
     Hkv, Dv = k.shape[1], v.shape[3]
     for t in (q, k, v):
         if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype):
@@ -58,9 +66,10 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                        dout: torch.Tensor, *, causal: bool = True, window: int = 0, scale: Optional[float] = None,
                        sink: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
                        max_seqlen: Optional[int] = None, group_mode: int = GQA_GROUP_TMEM,
-                       red_mode: int = GQA_RED_V4, deterministic: bool = False,
+                       red_mode: Optional[int] = None, deterministic: bool = False,
                        workspace: Optional[torch.Tensor] = None, out: Optional[dict] = None) -> dict:
-    """Returns dict(dq, dk, dv, delta[, dsink]).  `out` may hold preallocated tensors of the same names."""
+    """Returns dict(dq, dk, dv, delta[, dsink]).  `out` may hold preallocated tensors of the same names.
+    red_mode None picks :func:`preferred_red_mode`."""
     p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode, red_mode, deterministic)
     B, Hq, S, Dqk = q.shape
     Hkv, Dv = k.shape[1], v.shape[3]

@@ -113,8 +113,8 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc, d.need_dkdv_acc);
   uint8_t* base = static_cast<uint8_t*>(ws);
   pr.err = reinterpret_cast<int*>(base + d.ws.err_off);
-  pr.lse2 = reinterpret_cast<float*>(base + d.ws.lse2_off);
-  pr.delta_t = reinterpret_cast<float*>(base + d.ws.delta_off);
+  pr.nlse2 = reinterpret_cast<float*>(base + d.ws.lse2_off);
+  pr.ndelta = reinterpret_cast<float*>(base + d.ws.delta_off);
   pr.dq_acc = d.need_dq_acc ? reinterpret_cast<float*>(base + d.ws.dq_off) : nullptr;
   pr.dk_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dk_off) : nullptr;
   pr.dv_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dv_off) : nullptr;

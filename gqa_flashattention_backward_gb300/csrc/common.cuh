@@ -31,8 +31,9 @@ struct Problem {
   int* err;           // device error word (workspace)
   long long wait_limit;
   // workspace regions
-  float* lse2;        // [Hq][nseqs][ntiles][128]  LSE * log2(e), +inf on padding rows
-  float* delta_t;     // same layout, Delta, 0 on padding rows
+  float* nlse2;       // [Hq][nseqs][ntiles][128]  -LSE * log2(e), -inf on padding rows
+  float* ndelta;      // same layout, -Delta, 0 on padding rows (both negated so the
+                      // kernels use one packed fma / add per pair of elements)
   float* dq_acc;      // [B][Hq][S][Dqk] fp32
   float* dk_acc;      // [B][Hkv][S][Dqk] fp32
   float* dv_acc;      // [B][Hkv][S][Dv] fp32

@@ -88,8 +88,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
       delta[r] = acc;
       if (ok) {
         const size_t base = stat_index(p, h, s, il / kStatTile) + (il % kStatTile);
-        p.lse2[base] = __ldg(lse + r) * kLog2e;
-        p.delta_t[base] = acc;
+        p.nlse2[base] = -__ldg(lse + r) * kLog2e;
+        p.ndelta[base] = -acc;
       } else if (il == 0) {
         atomicCAS(p.err, 0, kErrSeqTooLong);
       }
@@ -98,8 +98,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
     if (ok && il == len - 1 && (len % kStatTile) != 0) {
       const size_t base = stat_index(p, h, s, il / kStatTile);
       for (int pr = (len % kStatTile) + sub; pr < kStatTile; pr += 8) {
-        p.lse2[base + pr] = __int_as_float(0x7f800000);  // +inf: exp2(x - inf) = 0
-        p.delta_t[base + pr] = 0.f;
+        p.nlse2[base + pr] = __int_as_float(0xff800000);  // -inf: exp2(x - inf) = 0
+        p.ndelta[base + pr] = 0.f;
       }
     }
     if (zero_dq) {

@@ -27,9 +27,10 @@
 // issue #4717 "atomic_add slows down attention backwards due to layout
 // conversions": vectorised atomics against scalar ones).
 //
-// Warp roles (320 threads): warps 0-3 softmax/dS warpgroup (thread r = key row r
-// = TMEM lane r); warps 4-7 dQ drain warpgroup (thread r = query row r); warp 8
-// TMA producer; warp 9 TMEM allocator + MMA issuer.
+// Warp roles (448 threads): warps 0-3 and 4-7 are two softmax/dS warpgroups
+// (thread r = key row r = TMEM lane r; the first takes query columns [0, BQ/2),
+// the second [BQ/2, BQ)); warps 8-11 dQ drain warpgroup (thread r = query row r);
+// warp 12 TMA producer; warp 13 TMEM allocator + MMA issuer.
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include <type_traits>
@@ -64,7 +65,9 @@ struct KvCfg {
   // TMEM columns
   static constexpr uint32_t T_S = 0, T_DP = BQ, T_DV = 2 * BQ, T_DK = 2 * BQ + DV;
   static constexpr uint32_t T_DQ = DQ_ALIAS ? T_DP : (T_DK + DQK);
-  static constexpr int THREADS = 320;
+  static constexpr int HALF = BQ / 2;                   // query columns per softmax warpgroup
+  static constexpr int NCH = HALF / 32;                   // 32-column chunks per softmax warpgroup
+  static constexpr int THREADS = 448;
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(T_DK + DQK <= 512 && (!HAS_DQ || DQ_ALIAS || T_DQ + DQK <= 512), "tmem");
 };
@@ -135,8 +138,20 @@ __device__ __forceinline__ void stage_and_reduce(uint8_t* stg, const CUtensorMap
   }
 }
 
+// One TMEM load of a warpgroup's half of the query columns (32 or 64 columns).
+template <int N>
+__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, uint32_t (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_half<64>(uint32_t taddr, uint32_t (&v)[64]) {
+  tmem_ld64(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_half<32>(uint32_t taddr, uint32_t (&v)[32]) {
+  tmem_ld32(taddr, v);
+}
+
 template <int DQK, int DV, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     kv_kernel(const Problem p, const __grid_constant__ Maps m, const int group_tmem, const int dq_mode,
               const int kv_mode, void* __restrict__ dk_out, void* __restrict__ dv_out) {
   using C = KvCfg<DQK, DV>;
@@ -175,8 +190,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&ctl.s_full, 1);
     mbar_init(&ctl.dp_full, 1);
-    mbar_init(&ctl.p_full, 128);
-    mbar_init(&ctl.ds_full, 128);
+    mbar_init(&ctl.p_full, 256);
+    mbar_init(&ctl.ds_full, 256);
     mbar_init(&ctl.dq_full, 1);
     mbar_init(&ctl.dq_empty, 128);
     mbar_init(&ctl.dsmem_free, 1);
@@ -184,7 +199,7 @@ __global__ void __launch_bounds__(320, 1)
     ctl.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(&ctl.tmem_base, 512);
     tmem_relinquish();
   }
@@ -194,7 +209,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = ctl.tmem_base;
   const WaitGuard guard{p.err, &ctl.abort_flag, p.wait_limit};
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_map(&m.q);
@@ -221,8 +236,8 @@ __global__ void __launch_bounds__(320, 1)
         mbar_expect_tx(&ctl.q_full[st], C::Q_BYTES + 2 * C::BQ * 4);
         for (int cb = 0; cb < DQK / 64; ++cb)
           tma_load_3d(sQ + cb * (C::BQ * 128), &m.q, &ctl.q_full[st], cb * 64, qrow, zq);
-        bulk_load(sL, p.lse2 + sidx, C::BQ * 4, &ctl.q_full[st]);
-        bulk_load(sD, p.delta_t + sidx, C::BQ * 4, &ctl.q_full[st]);
+        bulk_load(sL, p.nlse2 + sidx, C::BQ * 4, &ctl.q_full[st]);
+        bulk_load(sD, p.ndelta + sidx, C::BQ * 4, &ctl.q_full[st]);
         mbar_expect_tx(&ctl.do_full[st], C::DO_BYTES);
         for (int cb = 0; cb < DV / 64; ++cb)
           tma_load_3d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.do_full[st], cb * 64, qrow, zq);
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(128, C::BQ, BF16, false, false);
@@ -248,6 +263,11 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t aK = smem_u32(smem + C::OFF_K), aV = smem_u32(smem + C::OFF_V);
       const uint32_t aDS = smem_u32(smem + C::OFF_DS);
       const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
+      // packed 16-bit P^T / dS^T: each softmax warpgroup packs its half of the query
+      // columns into the first half of its own column range
+      auto a_col = [](int kk) -> uint32_t {
+        return static_cast<uint32_t>((kk / (C::HALF / 16)) * C::HALF + (kk % (C::HALF / 16)) * 8);
+      };
       bool ok = mbar_wait(&ctl.kv_full, 0, guard, 12);
       auto issue_s = [&](int it) -> bool {
         const int st = it % C::ST;
@@ -285,7 +305,7 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          umma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, sdesc_sw128(aDO + kk * 2048, C::BQ * 128, 1024), idDV,
+          umma_ts(tmem + C::T_DV, tmem + C::T_S + a_col(kk), sdesc_sw128(aDO + kk * 2048, C::BQ * 128, 1024), idDV,
                   (it > 0 || kk > 0) ? 1u : 0u);
         // next tile's S^T (its columns were read by the softmax warps, P^T was consumed by the dV MMA above)
         if (it + 1 < NIT && !issue_s(it + 1)) break;
@@ -294,7 +314,7 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          umma_ts(tmem + C::T_DK, tmem + C::T_DP + kk * 8, sdesc_sw128(aQ + kk * 2048, C::BQ * 128, 1024), idDK,
+          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), sdesc_sw128(aQ + kk * 2048, C::BQ * 128, 1024), idDK,
                   (it > 0 || kk > 0) ? 1u : 0u);
         // dQ_partial = dS . K
         if (dq_on) {
@@ -311,12 +331,12 @@ __global__ void __launch_bounds__(320, 1)
       }
       umma_commit(&ctl.acc_done);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ drain warpgroup
     if (C::HAS_DQ && dq_mode != kDqNone) {
-      const int r = tid - 128;  // query row within the tile == TMEM lane
-      const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-      uint8_t* stg = smem + C::OFF_STG + (warp - 4) * (2 * 32 * 32 * 4);
+      const int r = tid - 256;  // query row within the tile == TMEM lane
+      const uint32_t lane_base = static_cast<uint32_t>((warp - 8) * 32) << 16;
+      uint8_t* stg = smem + C::OFF_STG + (warp - 8) * (2 * 32 * 32 * 4);
       int nbulk = 0;
       for (int it = 0; it < NIT; ++it) {
         const int h = h_first + it / nt;
@@ -324,25 +344,25 @@ __global__ void __launch_bounds__(320, 1)
         const int il = t * C::BQ + r;
         if (!mbar_wait_warp(&ctl.dq_full, it & 1, guard, 19)) break;
         tc_fence_after();
-        uint32_t v[DQK / 32][32];
-#pragma unroll
-        for (int c = 0; c < DQK / 32; ++c) tmem_ld32(tmem + lane_base + C::T_DQ + 32 * c, v[c]);
-        tc_fence_before();
-        mbar_arrive(&ctl.dq_empty);
         const size_t grow = (static_cast<size_t>(sq.b) * p.Hq + h) * p.S + sq.start + il;
         const bool valid = il < sq.len;
 #pragma unroll
         for (int c = 0; c < DQK / 32; ++c) {
           const int c0 = 32 * c;
-          const uint32_t(&vc)[32] = v[c];
-          if (dq_mode == kDqRedV4) add_row32<kDqRedV4>(p.dq_acc, grow, DQK, c0, vc, valid);
-          else if (dq_mode == kDqScalar) add_row32<kDqScalar>(p.dq_acc, grow, DQK, c0, vc, valid);
-          else if (dq_mode == kDqStore) add_row32<kDqStore>(p.dq_acc, grow, DQK, c0, vc, valid);
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + C::T_DQ + c0, v);
+          if (c == DQK / 32 - 1) {  // every column is in registers: release the accumulator
+            tc_fence_before();
+            mbar_arrive(&ctl.dq_empty);
+          }
+          if (dq_mode == kDqRedV4) add_row32<kDqRedV4>(p.dq_acc, grow, DQK, c0, v, valid);
+          else if (dq_mode == kDqScalar) add_row32<kDqScalar>(p.dq_acc, grow, DQK, c0, v, valid);
+          else if (dq_mode == kDqStore) add_row32<kDqStore>(p.dq_acc, grow, DQK, c0, v, valid);
           else if (C::HAS_STAGING) {
             uint8_t* buf = stg + (nbulk & 1) * (32 * 32 * 4);
             if (lane == 0 && nbulk >= 1) bulk_wait_read1();
             __syncwarp();
-            stage_and_reduce(buf, &m.dq_acc, lane, vc, c0, sq.start + t * C::BQ + (warp - 4) * 32,
+            stage_and_reduce(buf, &m.dq_acc, lane, v, c0, sq.start + t * C::BQ + (warp - 8) * 32,
                              sq.b * p.Hq + h);
             ++nbulk;
           }
@@ -352,11 +372,13 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
     }
   } else {
-    // ------------------------------------------------------------ softmax / dS warpgroup
-    const int r = tid;                 // key row within the tile == TMEM lane
+    // ------------------------------------------------------------ softmax / dS warpgroups
+    const int wg = warp >> 2;          // which half of the query columns
+    const int r = tid & 127;           // key row within the tile == TMEM lane
     const int j = j0 + r;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const float sl2 = p.scale_log2;
+    const int cbase = wg * C::HALF;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
     bool ok = true;
     for (int it = 0; it < NIT; ++it) {
@@ -365,39 +387,50 @@ __global__ void __launch_bounds__(320, 1)
       const int i0 = t * C::BQ;
       const bool need_mask = (j0 + C::BK > sq.len) || (p.causal && i0 < j0 + C::BK - 1) ||
                              (p.window > 0 && i0 + C::BQ - 1 - j0 >= p.window);
-      const float* sL = reinterpret_cast<const float*>(smem + C::OFF_LSE) + st * C::BQ;
-      const float* sD = reinterpret_cast<const float*>(smem + C::OFF_DEL) + st * C::BQ;
+      const float4* sL4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE) + (st * C::BQ + cbase) / 4;
+      const float4* sD4 = reinterpret_cast<const float4*>(smem + C::OFF_DEL) + (st * C::BQ + cbase) / 4;
       if (!mbar_wait_warp(&ctl.q_full[st], (it / C::ST) & 1, guard, 20) ||
           !mbar_wait_warp(&ctl.s_full, it & 1, guard, 21)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // P^T = exp2(S^T * scale*log2e - LSE2), kept packed in registers for dS
-      uint32_t pk[C::BQ / 2];
+      // P^T = exp2(S^T * scale*log2e - LSE2) for this warpgroup's columns, kept packed (16-bit) for dS
+      uint32_t pk[C::HALF / 2];
+      uint32_t vs[C::HALF];
+      tmem_ld_half<C::HALF>(tmem + lane_base + C::T_S + cbase, vs);
 #pragma unroll
-      for (int c0 = 0; c0 < C::BQ; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::T_S + c0, v);
+      for (int c = 0; c < C::NCH; ++c) {
+        const uint32_t* v = vs + 32 * c;
+        float pf[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float a = ex2_approx(fmaf(__uint_as_float(v[2 * e]), sl2, -sL[c0 + 2 * e]));
-          float b = ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -sL[c0 + 2 * e + 1]));
-          if (need_mask) {
-            if (!kv_allowed(i0 + c0 + 2 * e, j, sq.len, p.causal, p.window)) a = 0.f;
-            if (!kv_allowed(i0 + c0 + 2 * e + 1, j, sq.len, p.causal, p.window)) b = 0.f;
-          }
-          pk[c0 / 2 + e] = pack2<BF16>(a, b);
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 l = sL4[8 * c + q4];
+          const float2 x0 = fma2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])), sl2,
+                                 make_float2(l.x, l.y));
+          const float2 x1 = fma2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])), sl2,
+                                 make_float2(l.z, l.w));
+          pf[4 * q4 + 0] = ex2_approx(x0.x);
+          pf[4 * q4 + 1] = ex2_approx(x0.y);
+          pf[4 * q4 + 2] = ex2_approx(x1.x);
+          pf[4 * q4 + 3] = ex2_approx(x1.y);
         }
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!kv_allowed(i0 + cbase + 32 * c + e, j, sq.len, p.causal, p.window)) pf[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[16 * c + e] = pack2<BF16>(pf[2 * e], pf[2 * e + 1]);
         uint32_t pc[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pc[e] = pk[c0 / 2 + e];
-        tmem_st16(tmem + lane_base + C::T_S + c0 / 2, pc);
+        for (int e = 0; e < 16; ++e) pc[e] = pk[16 * c + e];
+        tmem_st16(tmem + lane_base + C::T_S + cbase + 16 * c, pc);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl.p_full);
-      // dS^T = P^T * (dP^T - Delta)
+      // dS^T = P^T * (dP^T - Delta): the difference in fp32, the product on packed 16-bit pairs
       if (!mbar_wait_warp(&ctl.dp_full, it & 1, guard, 22)) {
         ok = false;
         break;
@@ -407,23 +440,25 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
+      tmem_ld_half<C::HALF>(tmem + lane_base + C::T_DP + cbase, vs);
 #pragma unroll
-      for (int c0 = 0; c0 < C::BQ; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + C::T_DP + c0, v);
+      for (int c = 0; c < C::NCH; ++c) {
+        const uint32_t* v = vs + 32 * c;
         uint32_t ds[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float2 pp;
-          if (BF16) pp = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c0 / 2 + e]));
-          else pp = __half22float2(*reinterpret_cast<const __half2*>(&pk[c0 / 2 + e]));
-          const float a = pp.x * (__uint_as_float(v[2 * e]) - sD[c0 + 2 * e]);
-          const float b = pp.y * (__uint_as_float(v[2 * e + 1]) - sD[c0 + 2 * e + 1]);
-          ds[e] = pack2<BF16>(a, b);
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 d = sD4[8 * c + q4];
+          const float2 a = add2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])),
+                                make_float2(d.x, d.y));
+          const float2 b = add2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])),
+                                make_float2(d.z, d.w));
+          ds[2 * q4] = mul_packed<BF16>(pk[16 * c + 2 * q4], pack2<BF16>(a.x, a.y));
+          ds[2 * q4 + 1] = mul_packed<BF16>(pk[16 * c + 2 * q4 + 1], pack2<BF16>(b.x, b.y));
         }
-        tmem_st16(tmem + lane_base + C::T_DP + c0 / 2, ds);
+        tmem_st16(tmem + lane_base + C::T_DP + cbase + 16 * c, ds);
         if (dq_on) {
           // dS for the dQ MMA: MN-major (query index contiguous), 128B swizzle, key row r = K index
+          const int c0 = cbase + 32 * c;
           uint8_t* sds = smem + C::OFF_DS + (c0 / 64) * (C::BK * 128) + r * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -438,6 +473,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(&ctl.ds_full);
     }
     // ---------------------------------------------------------- dK / dV epilogue
+    // warpgroup 0 writes dV, warpgroup 1 writes dK (both cover all 128 key rows)
     if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 24)) {
       tc_fence_after();
       const bool valid = j < sq.len;
@@ -474,13 +510,13 @@ __global__ void __launch_bounds__(320, 1)
             uint8_t* buf = stg + (nbulk & 1) * (32 * 32 * 4);
             if (lane == 0 && nbulk >= 1) bulk_wait_read1();
             __syncwarp();
-            stage_and_reduce(buf, map, lane, v, c0, sq.start + j0 + warp * 32, zk);
+            stage_and_reduce(buf, map, lane, v, c0, sq.start + j0 + (warp & 3) * 32, zk);
             ++nbulk;
           }
         }
       };
-      emit(C::T_DV, DV, dv_out, p.dv_acc, &m.dv_acc, 1.f);
-      emit(C::T_DK, DQK, dk_out, p.dk_acc, &m.dk_acc, p.scale);
+      if (wg == 0) emit(C::T_DV, DV, dv_out, p.dv_acc, &m.dv_acc, 1.f);
+      else emit(C::T_DK, DQK, dk_out, p.dk_acc, &m.dk_acc, p.scale);
       if (lane == 0 && nbulk > 0) bulk_wait0();
       __syncwarp();
     }
@@ -488,7 +524,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

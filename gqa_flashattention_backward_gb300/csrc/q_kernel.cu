@@ -328,8 +328,8 @@ __global__ void __launch_bounds__(192, 1)
     } else {
       // deterministic dQ pass
       const size_t sidx = stat_index(p, h, s, t) + r;
-      const float lse2 = p.lse2[sidx];
-      const float dlt = p.delta_t[sidx];
+      const float nlse2 = p.nlse2[sidx];
+      const float ndlt = p.ndelta[sidx];
       for (int it = 0; it < NIT; ++it) {
         const int kt = k0 + it;
         const int j0 = kt * C::BK;
@@ -349,14 +349,14 @@ __global__ void __launch_bounds__(192, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float pa = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, -lse2));
-            float pb = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, -lse2));
+            float pa = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, nlse2));
+            float pb = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, nlse2));
             if (need_mask) {
               if (!allowed(il, j0 + c0 + 2 * e, sq.len, p.causal, p.window)) pa = 0.f;
               if (!allowed(il, j0 + c0 + 2 * e + 1, sq.len, p.causal, p.window)) pb = 0.f;
             }
-            const float da = pa * (__uint_as_float(dv[2 * e]) - dlt);
-            const float db = pb * (__uint_as_float(dv[2 * e + 1]) - dlt);
+            const float da = pa * (__uint_as_float(dv[2 * e]) + ndlt);
+            const float db = pb * (__uint_as_float(dv[2 * e + 1]) + ndlt);
             pk[e] = pack2<BF16>(da, db);
           }
           tmem_st16(tP + c0 / 2, pk);

@@ -34,7 +34,7 @@ def problem_of(w) -> orc.Problem:
                        scale=w.resolved_scale, cu_seqlens=w.cu_seqlens)
 
 
-def gpu_run(w, inputs, *, group_mode=nat.GQA_GROUP_TMEM, red_mode=nat.GQA_RED_V4, deterministic=False,
+def gpu_run(w, inputs, *, group_mode=nat.GQA_GROUP_TMEM, red_mode=None, deterministic=False,
             o_lse=None):
     """Forward then backward on the GPU.  o_lse: optional (o, lse) CPU tensors to feed the backward."""
     q, k, v, do, sink = inputs
