@@ -299,6 +299,20 @@ def run_gpu(args):
                                      ws_.flops_exact() / (mms * 1e-3) / 1e12, 2))
             del cs
 
+    # the other workloads, same hot path and launch configuration (preprocess -> bwd -> postprocess [-> dsink])
+    configs = {}
+    if not args.no_configs:
+        for wc in (W.varlen(), W.sink_window(), W.long_context()):
+            cc = setup(wc)
+            nst = max(3, args.steps // 2)
+            ms, mms, _ = timed(cc, nst, args.warmup, main_events=True)
+            stp = ms / nst
+            configs[wc.name] = dict(shape=wc.describe(), tflops=round(wc.flops_convention() / (stp * 1e-3) / 1e12, 2),
+                                    tflops_exact=round(wc.flops_exact() / (stp * 1e-3) / 1e12, 2), ms=round(stp, 4),
+                                    main_kernels_ms=round(mms, 4),
+                                    frac_of_peak_exact=round(wc.flops_exact() / (stp * 1e-3) / 1e12 / peaks["bf16_tflops"], 4))
+            del cc
+
     line = None
     if rank == 0:
         cpu = None
@@ -316,7 +330,7 @@ def run_gpu(args):
                     flops_per_step_convention=flops_conv, flops_per_step_exact=flops_exact,
                     frac_of_peak_exact=round(flops_exact / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clocks,
-                    variants=variants, sweep=sweep)
+                    variants=variants, sweep=sweep, configs=configs)
         print(json.dumps(line), flush=True)
     if ws_n > 1:
         dist.barrier()
@@ -399,6 +413,7 @@ def main():
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
