@@ -260,24 +260,32 @@ __global__ void __launch_bounds__(448, 1)
       constexpr uint32_t idDV = idesc_f16(128, DV, BF16, false, true);
       constexpr uint32_t idDK = idesc_f16(128, DQK, BF16, false, true);
       constexpr uint32_t idDQ = idesc_f16(C::BQ, DQK, BF16, true, true);
-      const uint32_t aK = smem_u32(smem + C::OFF_K), aV = smem_u32(smem + C::OFF_V);
-      const uint32_t aDS = smem_u32(smem + C::OFF_DS);
       const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
       // packed 16-bit P^T / dS^T: each softmax warpgroup packs its half of the query
       // columns into the first half of its own column range
       auto a_col = [](int kk) -> uint32_t {
         return static_cast<uint32_t>((kk / (C::HALF / 16)) * C::HALF + (kk % (C::HALF / 16)) * 8);
       };
+      // shared-memory descriptors, built once and advanced by compile-time offsets
+      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);          // K tile, K-major
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::BK * 128, 1024); // K tile, MN-major
+      const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+      const uint64_t dDS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::BK * 128, 1024);
+      const uint64_t dQ_k0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      const uint64_t dQ_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::BQ * 128, 1024);
+      const uint64_t dDO_k0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+      const uint64_t dDO_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::BQ * 128, 1024);
+      // K-major operand with 64-element (128-byte) rows: K step kk lives in 64-column block kk/4 at byte kk%4*32
+      auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
       bool ok = mbar_wait(&ctl.kv_full, 0, guard, 12);
       auto issue_s = [&](int it) -> bool {
         const int st = it % C::ST;
         if (!mbar_wait(&ctl.q_full[st], (it / C::ST) & 1, guard, 13)) return false;
         tc_fence_after();
-        const uint32_t aQ = smem_u32(smem + C::OFF_Q + st * C::Q_BYTES);
+        const uint64_t dq = desc_advance(dQ_k0, st * C::Q_BYTES);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk)
-          umma_ss(tmem + C::T_S, sdesc_sw128(aK + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024),
-                  sdesc_sw128(aQ + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+          umma_ss(tmem + C::T_S, desc_advance(dK_k, kstep(kk, C::BK)), desc_advance(dq, kstep(kk, C::BQ)), idS, kk > 0);
         umma_commit(&ctl.s_full);
         return true;
       };
@@ -287,25 +295,24 @@ __global__ void __launch_bounds__(448, 1)
         // the dQ accumulator shares these columns: its drain must be finished
         if (C::DQ_ALIAS && dq_on && it >= 1 && !mbar_wait(&ctl.dq_empty, (it - 1) & 1, guard, 15)) return false;
         tc_fence_after();
-        const uint32_t aDO = smem_u32(smem + C::OFF_DO + st * C::DO_BYTES);
+        const uint64_t ddo = desc_advance(dDO_k0, st * C::DO_BYTES);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
-          umma_ss(tmem + C::T_DP, sdesc_sw128(aV + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024),
-                  sdesc_sw128(aDO + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+          umma_ss(tmem + C::T_DP, desc_advance(dV_k, kstep(kk, C::BK)), desc_advance(ddo, kstep(kk, C::BQ)), idS, kk > 0);
         umma_commit(&ctl.dp_full);
         return true;
       };
       if (ok && NIT > 0) ok = issue_s(0) && issue_dp(0);
       for (int it = 0; ok && it < NIT; ++it) {
         const int st = it % C::ST;
-        const uint32_t aQ = smem_u32(smem + C::OFF_Q + st * C::Q_BYTES);
-        const uint32_t aDO = smem_u32(smem + C::OFF_DO + st * C::DO_BYTES);
+        const uint64_t dq_mn = desc_advance(dQ_mn0, st * C::Q_BYTES);
+        const uint64_t ddo_mn = desc_advance(dDO_mn0, st * C::DO_BYTES);
         // dV += P^T . dO
         if (!mbar_wait(&ctl.p_full, it & 1, guard, 16)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          umma_ts(tmem + C::T_DV, tmem + C::T_S + a_col(kk), sdesc_sw128(aDO + kk * 2048, C::BQ * 128, 1024), idDV,
+          umma_ts(tmem + C::T_DV, tmem + C::T_S + a_col(kk), desc_advance(ddo_mn, kk * 2048), idDV,
                   (it > 0 || kk > 0) ? 1u : 0u);
         // next tile's S^T (its columns were read by the softmax warps, P^T was consumed by the dV MMA above)
         if (it + 1 < NIT && !issue_s(it + 1)) break;
@@ -314,15 +321,14 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), sdesc_sw128(aQ + kk * 2048, C::BQ * 128, 1024), idDK,
+          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_advance(dq_mn, kk * 2048), idDK,
                   (it > 0 || kk > 0) ? 1u : 0u);
         // dQ_partial = dS . K
         if (dq_on) {
           if (!C::DQ_ALIAS && it >= 1 && !mbar_wait(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
-            umma_ss(tmem + C::T_DQ, sdesc_sw128(aDS + kk * 2048, C::BK * 128, 1024),
-                    sdesc_sw128(aK + kk * 2048, C::BK * 128, 1024), idDQ, kk > 0);
+            umma_ss(tmem + C::T_DQ, desc_advance(dDS_mn, kk * 2048), desc_advance(dK_mn, kk * 2048), idDQ, kk > 0);
           umma_commit(&ctl.dq_full);
           umma_commit(&ctl.dsmem_free);
         }
@@ -381,7 +387,7 @@ __global__ void __launch_bounds__(448, 1)
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
     bool ok = true;
-    for (int it = 0; it < NIT; ++it) {
+    for (int it = 0; ok && it < NIT; ++it) {
       const int st = it % C::ST;
       const int t = t0 + it % nt;
       const int i0 = t * C::BQ;

@@ -160,6 +160,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// A descriptor for an address `bytes` further on: the start-address field holds
+// addr >> 4 in its low 14 bits and every operand lives below 256 KB of shared
+// memory, so the advance never carries out of the field.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Instruction descriptor, kind::f16 with fp32 accumulation.
 // a_mn / b_mn: operand is MN-major (M resp. N contiguous) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a_mn, bool b_mn) {
