@@ -29,9 +29,9 @@ __all__ = [
 
 
 def preferred_red_mode(Dqk: int) -> int:
-    """The fastest supported dQ reduction: the bulk tensor reduce where the tile has
-    shared-memory staging for it (head dim 64), vectorised red.v4 otherwise."""
-    return GQA_RED_BULK if Dqk == 64 else GQA_RED_V4
+    """The fastest measured reduction for every supported head dim: the bulk reduce of
+    whole tiles staged in shared memory."""
+    return GQA_RED_BULK
 
 
 def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=GQA_GROUP_TMEM,

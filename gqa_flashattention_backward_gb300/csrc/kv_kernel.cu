@@ -43,15 +43,18 @@ namespace gqa {
 template <int DQK, int DV>
 struct KvCfg {
   static constexpr int BK = 128;
-  static constexpr int BQ = (DQK == 192) ? 64 : 128;
+  static constexpr int BQ = (DQK == 64) ? 128 : 64;      // query rows per tile
   static constexpr bool HAS_DQ = (DQK != 192);          // (192,128): dQ from the query-stationary pass
-  static constexpr bool DQ_ALIAS = (DQK == 128);         // dQ accumulator shares the dP/dS columns
-  static constexpr bool HAS_STAGING = (DQK == 64);       // shared staging for the bulk dQ reduce
+  // d=128: dQ^T = K^T . dS^T with the head dim on the 128 TMEM lanes (a 64-row query tile cannot
+  // be the M of an MMA); the tile is transposed through shared memory for the reduction
+  static constexpr bool DQ_T = (DQK == 128);
+  static constexpr bool DQ_ALIAS = false;                // dQ accumulator shares the dP/dS columns
+  static constexpr bool HAS_STAGING = (DQK == 64);       // per-warp 32x32 staging for the bulk dQ reduce
   static constexpr int K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
   static constexpr int Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
-  static constexpr int ST = (DQK == 64) ? 3 : ((DQK == 128) ? 2 : 3);
+  static constexpr int ST = 3;
   static constexpr int DS_BYTES = HAS_DQ ? BQ * BK * 2 : 0;
-  static constexpr int STG_BYTES = HAS_STAGING ? 4 * 2 * 32 * 32 * 4 : 0;
+  static constexpr int STG_BYTES = HAS_STAGING ? 4 * 2 * 32 * 32 * 4 : (DQ_T ? BQ * DQK * 4 : 0);
   // shared-memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_K = 0, OFF_V = OFF_K + K_BYTES;
   static constexpr int OFF_Q = OFF_V + V_BYTES;                  // stage st at OFF_Q + st*Q_BYTES
@@ -64,12 +67,14 @@ struct KvCfg {
   static constexpr int SMEM = OFF_CTL + 256;
   // TMEM columns
   static constexpr uint32_t T_S = 0, T_DP = BQ, T_DV = 2 * BQ, T_DK = 2 * BQ + DV;
-  static constexpr uint32_t T_DQ = DQ_ALIAS ? T_DP : (T_DK + DQK);
+  static constexpr uint32_t T_DQ = DQ_ALIAS ? T_DP : (T_DK + DQK);  // dQ (DQK cols) or dQ^T (BQ cols)
   static constexpr int HALF = BQ / 2;                   // query columns per softmax warpgroup
   static constexpr int NCH = HALF / 32;                   // 32-column chunks per softmax warpgroup
   static constexpr int THREADS = 448;
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(T_DK + DQK <= 512 && (!HAS_DQ || DQ_ALIAS || T_DQ + DQK <= 512), "tmem");
+  static_assert(T_DK + DQK <= 512 && (!HAS_DQ || DQ_ALIAS || T_DQ + (DQ_T ? BQ : DQK) <= 512), "tmem");
+  // the dK/dV epilogue stages bulk reductions in the idle Q/dO stage buffers (8 warps x 8 KB)
+  static_assert(ST * (Q_BYTES + DO_BYTES) >= 8 * 2 * 32 * 32 * 4, "epilogue staging");
 };
 
 struct KvCtl {
@@ -259,7 +264,9 @@ __global__ void __launch_bounds__(448, 1)
       constexpr uint32_t idS = idesc_f16(128, C::BQ, BF16, false, false);
       constexpr uint32_t idDV = idesc_f16(128, DV, BF16, false, true);
       constexpr uint32_t idDK = idesc_f16(128, DQK, BF16, false, true);
-      constexpr uint32_t idDQ = idesc_f16(C::BQ, DQK, BF16, true, true);
+      // d=64: dQ = dS . K (M = query rows); d=128: dQ^T = K^T . dS^T (M = head dim)
+      constexpr uint32_t idDQ = C::DQ_T ? idesc_f16(128, C::BQ, BF16, true, true)
+                                        : idesc_f16(C::BQ, (DQK <= 256 ? DQK : 256), BF16, true, true);
       const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
       // packed 16-bit P^T / dS^T: each softmax warpgroup packs its half of the query
       // columns into the first half of its own column range
@@ -326,9 +333,17 @@ __global__ void __launch_bounds__(448, 1)
         // dQ_partial = dS . K
         if (dq_on) {
           if (!C::DQ_ALIAS && it >= 1 && !mbar_wait(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
+          if (C::DQ_T) {
+            // dQ^T = K^T . dS^T : A = K tile read MN-major, B = dS read MN-major (query contiguous)
 #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk)
-            umma_ss(tmem + C::T_DQ, desc_advance(dDS_mn, kk * 2048), desc_advance(dK_mn, kk * 2048), idDQ, kk > 0);
+            for (int kk = 0; kk < C::BK / 16; ++kk)
+              umma_ss(tmem + C::T_DQ, desc_advance(dK_mn, kk * 2048), desc_advance(dDS_mn, kk * 2048), idDQ, kk > 0);
+          } else {
+            // dQ = dS . K : A = dS read MN-major (query contiguous), B = K tile read MN-major
+#pragma unroll
+            for (int kk = 0; kk < C::BK / 16; ++kk)
+              umma_ss(tmem + C::T_DQ, desc_advance(dDS_mn, kk * 2048), desc_advance(dK_mn, kk * 2048), idDQ, kk > 0);
+          }
           umma_commit(&ctl.dq_full);
           umma_commit(&ctl.dsmem_free);
         }
@@ -350,6 +365,49 @@ __global__ void __launch_bounds__(448, 1)
         const int il = t * C::BQ + r;
         if (!mbar_wait_warp(&ctl.dq_full, it & 1, guard, 19)) break;
         tc_fence_after();
+        if (C::DQ_T) {
+          // thread r = head-dim column r: the tile is transposed through shared memory
+          float* tst = reinterpret_cast<float*>(smem + C::OFF_STG);  // [BQ query rows][DQK]
+          uint32_t v[C::BQ];
+          tmem_ld_half<C::BQ>(tmem + lane_base + C::T_DQ, v);
+          tc_fence_before();
+          mbar_arrive(&ctl.dq_empty);
+          if (r == 0 && nbulk > 0) bulk_wait_read0();  // the previous tile's reduce has read the staging
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int i = 0; i < C::BQ; ++i) tst[i * DQK + r] = __uint_as_float(v[i]);
+          const int row0 = t * C::BQ;
+          const int nvalid = sq.len - row0 < C::BQ ? sq.len - row0 : C::BQ;
+          float* gdst = p.dq_acc + ((static_cast<size_t>(sq.b) * p.Hq + h) * p.S + sq.start + row0) * DQK;
+          if (dq_mode == kDqBulk) {
+            fence_async_smem();
+            named_bar_sync(1, 128);
+            if (r == 0) {  // the tile's rows are contiguous in the accumulator: one bulk reduce
+              bulk_reduce_add_f32(gdst, tst, static_cast<uint32_t>(nvalid) * DQK * 4);
+              bulk_commit();
+            }
+            ++nbulk;
+          } else {
+            named_bar_sync(1, 128);
+            const float4* s4 = reinterpret_cast<const float4*>(tst);
+            for (int idx = r; idx < nvalid * (DQK / 4); idx += 128) {
+              const float4 x = s4[idx];
+              float* dst = gdst + 4 * idx;
+              if (dq_mode == kDqRedV4) {
+                red_add_v4(dst, x.x, x.y, x.z, x.w);
+              } else if (dq_mode == kDqScalar) {
+                red_add_f32(dst, x.x);
+                red_add_f32(dst + 1, x.y);
+                red_add_f32(dst + 2, x.z);
+                red_add_f32(dst + 3, x.w);
+              } else {
+                *reinterpret_cast<float4*>(dst) = x;
+              }
+            }
+            named_bar_sync(1, 128);  // staging free for the next tile
+          }
+          continue;
+        }
         const size_t grow = (static_cast<size_t>(sq.b) * p.Hq + h) * p.S + sq.start + il;
         const bool valid = il < sq.len;
 #pragma unroll
@@ -374,7 +432,7 @@ __global__ void __launch_bounds__(448, 1)
           }
         }
       }
-      if (lane == 0 && nbulk > 0) bulk_wait0();
+      if (nbulk > 0 && (C::DQ_T ? r == 0 : lane == 0)) bulk_wait0();
       __syncwarp();
     }
   } else {
@@ -562,7 +620,7 @@ cudaError_t launch_bwd_kv(const Problem& p, int dtype_bf16, const Maps& m, const
 }
 
 bool kv_kernel_has_dq(int Dqk) { return Dqk != 192; }
-bool kv_kernel_has_bulk_dq(int Dqk) { return Dqk == 64; }
-int kv_kernel_bq(int Dqk) { return Dqk == 192 ? 64 : 128; }
+bool kv_kernel_has_bulk_dq(int Dqk) { return Dqk != 192; }
+int kv_kernel_bq(int Dqk) { return Dqk == 64 ? 128 : 64; }
 
 }  // namespace gqa

@@ -101,10 +101,9 @@ def test_packed_sequence_rules(lib):
 
 
 def test_bulk_reduce_support_matrix(lib):
-    assert nat.workspace_size(_p(red_mode=nat.GQA_RED_BULK)) > 0
-    assert nat.workspace_size(_p(Dqk=128, Dv=128, red_mode=nat.GQA_RED_BULK)) == 0
-    assert nat.workspace_size(_p(Dqk=128, Dv=128, red_mode=nat.GQA_RED_BULK, deterministic=True)) > 0
-    assert nat.workspace_size(_p(Dqk=192, Dv=128, red_mode=nat.GQA_RED_BULK)) > 0
+    for dqk, dv in ((64, 64), (128, 128), (192, 128)):
+        for det in (False, True):
+            assert nat.workspace_size(_p(Dqk=dqk, Dv=dv, red_mode=nat.GQA_RED_BULK, deterministic=det)) > 0
 
 
 def test_strerror(lib):

@@ -67,16 +67,10 @@ MODES = {
 }
 
 
-def _mode_supported(w, mode):
-    return not (MODES[mode].get("red_mode") == nat.GQA_RED_BULK and w.Dqk == 128)
-
-
 @pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("name", list(CASES))
 def test_backward(name, mode):
     w = CASES[name]
-    if not _mode_supported(w, mode):
-        pytest.skip("bulk dQ reduction is not built for head dim 128")
     inputs, ref = _oracle(name)
     res = gpu_run(w, inputs, **MODES[mode])
     _compare(w, res, ref)
