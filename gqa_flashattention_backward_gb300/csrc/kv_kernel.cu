@@ -466,26 +466,42 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c) {
         const uint32_t* v = vs + 32 * c;
-        float pf[32];
+        if (BF16) {
+          float pf[32];
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 l = sL4[8 * c + q4];
-          const float2 x0 = fma2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])), sl2,
-                                 make_float2(l.x, l.y));
-          const float2 x1 = fma2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])), sl2,
-                                 make_float2(l.z, l.w));
-          pf[4 * q4 + 0] = ex2_approx(x0.x);
-          pf[4 * q4 + 1] = ex2_approx(x0.y);
-          pf[4 * q4 + 2] = ex2_approx(x1.x);
-          pf[4 * q4 + 3] = ex2_approx(x1.y);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 l = sL4[8 * c + q4];
+            const float2 x0 = fma2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])), sl2,
+                                   make_float2(l.x, l.y));
+            const float2 x1 = fma2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])), sl2,
+                                   make_float2(l.z, l.w));
+            pf[4 * q4 + 0] = ex2_approx(x0.x);
+            pf[4 * q4 + 1] = ex2_approx(x0.y);
+            pf[4 * q4 + 2] = ex2_approx(x1.x);
+            pf[4 * q4 + 3] = ex2_approx(x1.y);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[16 * c + e] = pack2<true>(pf[2 * e], pf[2 * e + 1]);
+        } else {
+          // fp16: the exponent argument is rounded to fp16 and exponentiated two at a time; the
+          // result is the packed P the MMA consumes (argument rounding adds at most ~2e-4 to P)
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 l = sL4[8 * c + q4];
+            const float2 x0 = fma2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])), sl2,
+                                   make_float2(l.x, l.y));
+            const float2 x1 = fma2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])), sl2,
+                                   make_float2(l.z, l.w));
+            pk[16 * c + 2 * q4] = ex2_f16x2(pack2<false>(x0.x, x0.y));
+            pk[16 * c + 2 * q4 + 1] = ex2_f16x2(pack2<false>(x1.x, x1.y));
+          }
         }
         if (need_mask) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (!kv_allowed(i0 + cbase + 32 * c + e, j, sq.len, p.causal, p.window)) pf[e] = 0.f;
+            if (!kv_allowed(i0 + cbase + 32 * c + e, j, sq.len, p.causal, p.window))
+              pk[16 * c + e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
         }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[16 * c + e] = pack2<BF16>(pf[2 * e], pf[2 * e + 1]);
         uint32_t pc[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pc[e] = pk[16 * c + e];
