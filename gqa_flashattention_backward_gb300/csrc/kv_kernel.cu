@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(448, 1)
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the issue loop; one elected lane issues each MMA
       constexpr uint32_t idS = idesc_f16(128, C::BQ, BF16, false, false);
       constexpr uint32_t idDV = idesc_f16(128, DV, BF16, false, true);
       constexpr uint32_t idDK = idesc_f16(128, DQK, BF16, false, true);
@@ -284,10 +284,10 @@ __global__ void __launch_bounds__(448, 1)
       const uint64_t dDO_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::BQ * 128, 1024);
       // K-major operand with 64-element (128-byte) rows: K step kk lives in 64-column block kk/4 at byte kk%4*32
       auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
-      bool ok = mbar_wait(&ctl.kv_full, 0, guard, 12);
+      bool ok = mbar_wait_warp(&ctl.kv_full, 0, guard, 12);
       auto issue_s = [&](int it) -> bool {
         const int st = it % C::ST;
-        if (!mbar_wait(&ctl.q_full[st], (it / C::ST) & 1, guard, 13)) return false;
+        if (!mbar_wait_warp(&ctl.q_full[st], (it / C::ST) & 1, guard, 13)) return false;
         tc_fence_after();
         const uint64_t dq = desc_advance(dQ_k0, st * C::Q_BYTES);
 #pragma unroll
@@ -298,9 +298,9 @@ __global__ void __launch_bounds__(448, 1)
       };
       auto issue_dp = [&](int it) -> bool {
         const int st = it % C::ST;
-        if (!mbar_wait(&ctl.do_full[st], (it / C::ST) & 1, guard, 14)) return false;
+        if (!mbar_wait_warp(&ctl.do_full[st], (it / C::ST) & 1, guard, 14)) return false;
         // the dQ accumulator shares these columns: its drain must be finished
-        if (C::DQ_ALIAS && dq_on && it >= 1 && !mbar_wait(&ctl.dq_empty, (it - 1) & 1, guard, 15)) return false;
+        if (C::DQ_ALIAS && dq_on && it >= 1 && !mbar_wait_warp(&ctl.dq_empty, (it - 1) & 1, guard, 15)) return false;
         tc_fence_after();
         const uint64_t ddo = desc_advance(dDO_k0, st * C::DO_BYTES);
 #pragma unroll
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(448, 1)
         const uint64_t dq_mn = desc_advance(dQ_mn0, st * C::Q_BYTES);
         const uint64_t ddo_mn = desc_advance(dDO_mn0, st * C::DO_BYTES);
         // dV += P^T . dO
-        if (!mbar_wait(&ctl.p_full, it & 1, guard, 16)) break;
+        if (!mbar_wait_warp(&ctl.p_full, it & 1, guard, 16)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(448, 1)
         // next tile's S^T (its columns were read by the softmax warps, P^T was consumed by the dV MMA above)
         if (it + 1 < NIT && !issue_s(it + 1)) break;
         // dK += dS^T . Q
-        if (!mbar_wait(&ctl.ds_full, it & 1, guard, 17)) break;
+        if (!mbar_wait_warp(&ctl.ds_full, it & 1, guard, 17)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(448, 1)
                   (it > 0 || kk > 0) ? 1u : 0u);
         // dQ_partial = dS . K
         if (dq_on) {
-          if (!C::DQ_ALIAS && it >= 1 && !mbar_wait(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
+          if (!C::DQ_ALIAS && it >= 1 && !mbar_wait_warp(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
           if (C::DQ_T) {
             // dQ^T = K^T . dS^T : A = K tile read MN-major, B = dS read MN-major (query contiguous)
 #pragma unroll

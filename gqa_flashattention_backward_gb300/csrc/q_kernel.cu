@@ -154,16 +154,16 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the issue loop; one elected lane issues each MMA
       constexpr uint32_t idS = idesc_f16(128, C::BK, BF16, false, false);
       constexpr uint32_t idPV = idesc_f16(128, DV, BF16, false, true);
       constexpr uint32_t idDQ = idesc_f16(128, DQK, BF16, false, true);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-      bool ok = mbar_wait(&ctl.bar_q, 0, guard, 2);
+      bool ok = mbar_wait_warp(&ctl.bar_q, 0, guard, 2);
       int pending = -1;  // output-pass tile whose P.V is not issued yet
       auto issue_pv = [&](int j) -> bool {
         const int u = j - n;
-        if (!mbar_wait(&ctl.p_full[u & 1], (u >> 1) & 1, guard, 5)) return false;
+        if (!mbar_wait_warp(&ctl.p_full[u & 1], (u >> 1) & 1, guard, 5)) return false;
         tc_fence_after();
         const uint32_t tP = tmem + ((j & 1) ? C::T_S1 : C::T_S0);
         const uint32_t aVj = smem_u32(sK0 + (j % C::KST) * C::STAGE_BYTES) + C::K_BYTES;
@@ -178,10 +178,10 @@ __global__ void __launch_bounds__(192, 1)
         const int st = it % C::KST;
         const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
         const uint32_t aV = aK + C::K_BYTES;
-        if (!mbar_wait(&ctl.kv_full[st], (it / C::KST) & 1, guard, 3)) break;
+        if (!mbar_wait_warp(&ctl.kv_full[st], (it / C::KST) & 1, guard, 3)) break;
         if (FWD) {
           const int buf = it & 1;
-          if (it >= 2 && !mbar_wait(&ctl.s_free[buf], ((it - 2) >> 1) & 1, guard, 4)) break;
+          if (it >= 2 && !mbar_wait_warp(&ctl.s_free[buf], ((it - 2) >> 1) & 1, guard, 4)) break;
           tc_fence_after();
           const uint32_t tS = tmem + (buf ? C::T_S1 : C::T_S0);
 #pragma unroll
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           if (it >= n) pending = it;
         } else {
-          if (it >= 1 && !mbar_wait(&ctl.s_free[0], (it - 1) & 1, guard, 4)) break;
+          if (it >= 1 && !mbar_wait_warp(&ctl.s_free[0], (it - 1) & 1, guard, 4)) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk)
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(192, 1)
             umma_ss(tmem + C::T_S1, sdesc_sw128(aDO + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024),
                     sdesc_sw128(aV + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
           umma_commit(&ctl.s_full[0]);
-          if (!mbar_wait(&ctl.p_full[0], it & 1, guard, 5)) break;
+          if (!mbar_wait_warp(&ctl.p_full[0], it & 1, guard, 5)) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
