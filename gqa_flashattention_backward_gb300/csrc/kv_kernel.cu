@@ -53,14 +53,14 @@ struct KvCfg {
   static constexpr int K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
   static constexpr int Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
   static constexpr int ST = 3;
-  static constexpr int DS_BYTES = HAS_DQ ? BQ * BK * 2 : 0;
-  static constexpr int STG_BYTES = HAS_STAGING ? 4 * 2 * 32 * 32 * 4 : (DQ_T ? BQ * DQK * 4 : 0);
+  static constexpr int DS_BYTES = HAS_DQ ? BQ * BK * 2 : 0;   // one dS tile; two alternate
+  static constexpr int STG_BYTES = HAS_STAGING ? 4 * 32 * 32 * 4 : (DQ_T ? BQ * DQK * 4 : 0);
   // shared-memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_K = 0, OFF_V = OFF_K + K_BYTES;
   static constexpr int OFF_Q = OFF_V + V_BYTES;                  // stage st at OFF_Q + st*Q_BYTES
   static constexpr int OFF_DO = OFF_Q + ST * Q_BYTES;
   static constexpr int OFF_DS = OFF_DO + ST * DO_BYTES;
-  static constexpr int OFF_STG = OFF_DS + DS_BYTES;
+  static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
   static constexpr int OFF_LSE = OFF_STG + STG_BYTES;           // ST x BQ floats
   static constexpr int OFF_DEL = OFF_LSE + ST * BQ * 4;
   static constexpr int OFF_CTL = OFF_DEL + ST * BQ * 4;
@@ -68,11 +68,15 @@ struct KvCfg {
   // TMEM columns
   static constexpr uint32_t T_S = 0, T_DP = BQ, T_DV = 2 * BQ, T_DK = 2 * BQ + DV;
   static constexpr uint32_t T_DQ = DQ_ALIAS ? T_DP : (T_DK + DQK);  // dQ (DQK cols) or dQ^T (BQ cols)
+  // packed dS^T (BQ/2 columns) in the 64 columns every head-dim configuration leaves free, so the
+  // next tile's dP^T can be computed while dK still reads this tile's dS^T
+  static constexpr uint32_t T_DSP = 448;
   static constexpr int HALF = BQ / 2;                   // query columns per softmax warpgroup
   static constexpr int NCH = HALF / 32;                   // 32-column chunks per softmax warpgroup
   static constexpr int THREADS = 448;
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(T_DK + DQK <= 512 && (!HAS_DQ || DQ_ALIAS || T_DQ + (DQ_T ? BQ : DQK) <= 512), "tmem");
+  static_assert(T_DK + DQK <= T_DSP && (!HAS_DQ || DQ_ALIAS || T_DQ + (DQ_T ? BQ : DQK) <= T_DSP), "tmem");
+  static_assert(T_DSP + BQ / 2 <= 512, "tmem");
   // the dK/dV epilogue stages bulk reductions in the idle Q/dO stage buffers (8 warps x 8 KB)
   static_assert(ST * (Q_BYTES + DO_BYTES) >= 8 * 2 * 32 * 32 * 4, "epilogue staging");
 };
@@ -80,8 +84,8 @@ struct KvCfg {
 struct KvCtl {
   uint64_t kv_full;
   uint64_t q_full[3], do_full[3], q_empty[3];
-  uint64_t s_full, dp_full, p_full, ds_full;
-  uint64_t dq_full, dq_empty, dsmem_free, acc_done;
+  uint64_t s_full, dp_full, p_full, ds_full, ds_free;
+  uint64_t dq_full, dq_empty, dsmem_free[2], acc_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -185,7 +189,9 @@ __global__ void __launch_bounds__(448, 1)
   const int j0 = kt * C::BK;
   const int zk = sq.b * p.Hkv + g;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the warp index goes through a shuffle so the compiler knows it is warp-uniform: the warp-role
+  // branches below are then uniform and the MMA operands can stay in uniform registers
+  const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
   if (tid == 0) {
     mbar_init(&ctl.kv_full, 1);
     for (int i = 0; i < C::ST; ++i) {
@@ -195,11 +201,13 @@ __global__ void __launch_bounds__(448, 1)
     }
     mbar_init(&ctl.s_full, 1);
     mbar_init(&ctl.dp_full, 1);
-    mbar_init(&ctl.p_full, 256);
-    mbar_init(&ctl.ds_full, 256);
+    mbar_init(&ctl.p_full, 8);   // one arrival per softmax warp
+    mbar_init(&ctl.ds_full, 8);
+    mbar_init(&ctl.ds_free, 1);
     mbar_init(&ctl.dq_full, 1);
-    mbar_init(&ctl.dq_empty, 128);
-    mbar_init(&ctl.dsmem_free, 1);
+    mbar_init(&ctl.dq_empty, 4);  // one arrival per drain warp
+    mbar_init(&ctl.dsmem_free[0], 1);
+    mbar_init(&ctl.dsmem_free[1], 1);
     mbar_init(&ctl.acc_done, 1);
     ctl.abort_flag = 0;
     fence_mbar_init();
@@ -211,7 +219,9 @@ __global__ void __launch_bounds__(448, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = ctl.tmem_base;
+  // broadcast from lane 0 so the compiler treats the TMEM base as warp-uniform (uniform registers
+  // for the MMA operands instead of per-MMA register moves)
+  const uint32_t tmem = __shfl_sync(0xffffffffu, ctl.tmem_base, 0);
   const WaitGuard guard{p.err, &ctl.abort_flag, p.wait_limit};
 
   if (warp == 12) {
@@ -323,32 +333,34 @@ __global__ void __launch_bounds__(448, 1)
                   (it > 0 || kk > 0) ? 1u : 0u);
         // next tile's S^T (its columns were read by the softmax warps, P^T was consumed by the dV MMA above)
         if (it + 1 < NIT && !issue_s(it + 1)) break;
-        // dK += dS^T . Q
+        // the softmax warps are idle until the next tile's dP^T: it goes first, then dK += dS^T . Q
         if (!mbar_wait_warp(&ctl.ds_full, it & 1, guard, 17)) break;
+        if (it + 1 < NIT && !issue_dp(it + 1)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_advance(dq_mn, kk * 2048), idDK,
+          umma_ts(tmem + C::T_DK, tmem + C::T_DSP + kk * 8, desc_advance(dq_mn, kk * 2048), idDK,
                   (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&ctl.ds_free);
         // dQ_partial = dS . K
         if (dq_on) {
           if (!C::DQ_ALIAS && it >= 1 && !mbar_wait_warp(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
+          const uint32_t ds_off = (it & 1) * C::DS_BYTES;  // dS tiles alternate between two buffers
           if (C::DQ_T) {
             // dQ^T = K^T . dS^T : A = K tile read MN-major, B = dS read MN-major (query contiguous)
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
-              umma_ss(tmem + C::T_DQ, desc_advance(dK_mn, kk * 2048), desc_advance(dDS_mn, kk * 2048), idDQ, kk > 0);
+              umma_ss(tmem + C::T_DQ, desc_advance(dK_mn, kk * 2048), desc_advance(dDS_mn, ds_off + kk * 2048), idDQ, kk > 0);
           } else {
             // dQ = dS . K : A = dS read MN-major (query contiguous), B = K tile read MN-major
 #pragma unroll
             for (int kk = 0; kk < C::BK / 16; ++kk)
-              umma_ss(tmem + C::T_DQ, desc_advance(dDS_mn, kk * 2048), desc_advance(dK_mn, kk * 2048), idDQ, kk > 0);
+              umma_ss(tmem + C::T_DQ, desc_advance(dDS_mn, ds_off + kk * 2048), desc_advance(dK_mn, kk * 2048), idDQ, kk > 0);
           }
           umma_commit(&ctl.dq_full);
-          umma_commit(&ctl.dsmem_free);
+          umma_commit(&ctl.dsmem_free[it & 1]);
         }
         umma_commit(&ctl.q_empty[st]);
-        if (it + 1 < NIT && !issue_dp(it + 1)) break;
       }
       umma_commit(&ctl.acc_done);
     }
@@ -357,7 +369,7 @@ __global__ void __launch_bounds__(448, 1)
     if (C::HAS_DQ && dq_mode != kDqNone) {
       const int r = tid - 256;  // query row within the tile == TMEM lane
       const uint32_t lane_base = static_cast<uint32_t>((warp - 8) * 32) << 16;
-      uint8_t* stg = smem + C::OFF_STG + (warp - 8) * (2 * 32 * 32 * 4);
+      uint8_t* stg = smem + C::OFF_STG + (warp - 8) * (32 * 32 * 4);
       int nbulk = 0;
       for (int it = 0; it < NIT; ++it) {
         const int h = h_first + it / nt;
@@ -371,7 +383,7 @@ __global__ void __launch_bounds__(448, 1)
           uint32_t v[C::BQ];
           tmem_ld_half<C::BQ>(tmem + lane_base + C::T_DQ, v);
           tc_fence_before();
-          mbar_arrive(&ctl.dq_empty);
+          mbar_arrive_warp(&ctl.dq_empty);
           if (r == 0 && nbulk > 0) bulk_wait_read0();  // the previous tile's reduce has read the staging
           named_bar_sync(1, 128);
 #pragma unroll
@@ -408,6 +420,28 @@ __global__ void __launch_bounds__(448, 1)
           }
           continue;
         }
+        if constexpr (C::HAS_STAGING) {
+          if (dq_mode == kDqBulk) {
+            // the whole row into registers, release the accumulator, then stage and reduce each
+            // 32-column chunk through this warp's single staging buffer
+            uint32_t v[DQK];
+            tmem_ld_half<DQK>(tmem + lane_base + C::T_DQ, v);
+            tc_fence_before();
+            mbar_arrive_warp(&ctl.dq_empty);
+#pragma unroll
+            for (int c = 0; c < DQK / 32; ++c) {
+              uint32_t w[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) w[e] = v[32 * c + e];
+              if (lane == 0 && nbulk >= 1) bulk_wait_read0();  // the previous reduce has read the buffer
+              __syncwarp();
+              stage_and_reduce(stg, &m.dq_acc, lane, w, 32 * c, sq.start + t * C::BQ + (warp - 8) * 32,
+                               sq.b * p.Hq + h);
+              ++nbulk;
+            }
+            continue;
+          }
+        }
         const size_t grow = (static_cast<size_t>(sq.b) * p.Hq + h) * p.S + sq.start + il;
         const bool valid = il < sq.len;
 #pragma unroll
@@ -417,19 +451,11 @@ __global__ void __launch_bounds__(448, 1)
           tmem_ld32(tmem + lane_base + C::T_DQ + c0, v);
           if (c == DQK / 32 - 1) {  // every column is in registers: release the accumulator
             tc_fence_before();
-            mbar_arrive(&ctl.dq_empty);
+            mbar_arrive_warp(&ctl.dq_empty);
           }
           if (dq_mode == kDqRedV4) add_row32<kDqRedV4>(p.dq_acc, grow, DQK, c0, v, valid);
           else if (dq_mode == kDqScalar) add_row32<kDqScalar>(p.dq_acc, grow, DQK, c0, v, valid);
           else if (dq_mode == kDqStore) add_row32<kDqStore>(p.dq_acc, grow, DQK, c0, v, valid);
-          else if (C::HAS_STAGING) {
-            uint8_t* buf = stg + (nbulk & 1) * (32 * 32 * 4);
-            if (lane == 0 && nbulk >= 1) bulk_wait_read1();
-            __syncwarp();
-            stage_and_reduce(buf, &m.dq_acc, lane, v, c0, sq.start + t * C::BQ + (warp - 8) * 32,
-                             sq.b * p.Hq + h);
-            ++nbulk;
-          }
         }
       }
       if (nbulk > 0 && (C::DQ_T ? r == 0 : lane == 0)) bulk_wait0();
@@ -509,13 +535,18 @@ __global__ void __launch_bounds__(448, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ctl.p_full);
+      mbar_arrive_warp(&ctl.p_full);
       // dS^T = P^T * (dP^T - Delta): the difference in fp32, the product on packed 16-bit pairs
       if (!mbar_wait_warp(&ctl.dp_full, it & 1, guard, 22)) {
         ok = false;
         break;
       }
-      if (dq_on && it >= 1 && !mbar_wait_warp(&ctl.dsmem_free, (it - 1) & 1, guard, 23)) {
+      if (dq_on && it >= 2 && !mbar_wait_warp(&ctl.dsmem_free[it & 1], ((it - 2) >> 1) & 1, guard, 23)) {
+        ok = false;
+        break;
+      }
+      // the previous tile's dK MMA must have read its dS^T before this one is stored
+      if (it >= 1 && !mbar_wait_warp(&ctl.ds_free, (it - 1) & 1, guard, 25)) {
         ok = false;
         break;
       }
@@ -535,11 +566,11 @@ __global__ void __launch_bounds__(448, 1)
           ds[2 * q4] = mul_packed<BF16>(pk[16 * c + 2 * q4], pack2<BF16>(a.x, a.y));
           ds[2 * q4 + 1] = mul_packed<BF16>(pk[16 * c + 2 * q4 + 1], pack2<BF16>(b.x, b.y));
         }
-        tmem_st16(tmem + lane_base + C::T_DP + cbase + 16 * c, ds);
+        tmem_st16(tmem + lane_base + C::T_DSP + cbase / 2 + 16 * c, ds);
         if (dq_on) {
           // dS for the dQ MMA: MN-major (query index contiguous), 128B swizzle, key row r = K index
           const int c0 = cbase + 32 * c;
-          uint8_t* sds = smem + C::OFF_DS + (c0 / 64) * (C::BK * 128) + r * 128;
+          uint8_t* sds = smem + C::OFF_DS + (it & 1) * C::DS_BYTES + (c0 / 64) * (C::BK * 128) + r * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int chunk = ((c0 % 64) / 8 + q) ^ (r & 7);
@@ -550,7 +581,7 @@ __global__ void __launch_bounds__(448, 1)
       tmem_st_wait();
       if (dq_on) fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&ctl.ds_full);
+      mbar_arrive_warp(&ctl.ds_full);
     }
     // ---------------------------------------------------------- dK / dV epilogue
     // warpgroup 0 writes dV, warpgroup 1 writes dK (both cover all 128 key rows)

@@ -89,7 +89,9 @@ __global__ void __launch_bounds__(192, 1)
   const int zq = sq.b * p.Hq + h, zk = sq.b * p.Hkv + g;
   const int row0 = sq.start + t * C::BQ;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the warp index goes through a shuffle so the compiler knows it is warp-uniform: the warp-role
+  // branches below are then uniform and the MMA operands can stay in uniform registers
+  const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
   if (tid == 0) {
     mbar_init(&ctl.bar_q, 1);
     for (int i = 0; i < C::KST; ++i) {
@@ -98,8 +100,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.s_free[i], 128);
-      mbar_init(&ctl.p_full[i], 128);
+      mbar_init(&ctl.s_free[i], 4);  // one arrival per softmax warp
+      mbar_init(&ctl.p_full[i], 4);
     }
     mbar_init(&ctl.acc_done, 1);
     ctl.abort_flag = 0;
@@ -112,7 +114,9 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = ctl.tmem_base;
+  // broadcast from lane 0 so the compiler treats the TMEM base as warp-uniform (uniform registers
+  // for the MMA operands instead of per-MMA register moves)
+  const uint32_t tmem = __shfl_sync(0xffffffffu, ctl.tmem_base, 0);
   const WaitGuard guard{p.err, &ctl.abort_flag, p.wait_limit};
 
   if (warp == 4) {
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
           tc_fence_before();
-          mbar_arrive(&ctl.s_free[buf]);
+          mbar_arrive_warp(&ctl.s_free[buf]);
           if (it == n - 1) lse2 = (l > 0.f) ? mx + log2f(l) : INFINITY;
         } else {
           // output pass: P = exp2(S*scale*log2e - LSE2), packed in place over S
@@ -294,8 +298,8 @@ __global__ void __launch_bounds__(192, 1)
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&ctl.p_full[u & 1]);
-          mbar_arrive(&ctl.s_free[buf]);
+          mbar_arrive_warp(&ctl.p_full[u & 1]);
+          mbar_arrive_warp(&ctl.s_free[buf]);
         }
       }
       if (n == 0) lse2 = (l > 0.f) ? mx + log2f(l) : INFINITY;
@@ -363,8 +367,8 @@ __global__ void __launch_bounds__(192, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&ctl.p_full[0]);
-        mbar_arrive(&ctl.s_free[0]);
+        mbar_arrive_warp(&ctl.p_full[0]);
+        mbar_arrive_warp(&ctl.s_free[0]);
       }
       if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
         tc_fence_after();
