@@ -102,6 +102,14 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const vo
       "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// Same box as tma_reduce_add_3d, plain store (the no-accumulation benchmark mode).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_wait_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
@@ -133,7 +141,7 @@ __device__ __forceinline__ void add_row32(float* acc, size_t grow, int ld, int c
 // Bulk path: stage a warp's 32x32 fp32 block in 128B-swizzled shared memory
 // (the layout the fp32 reduce tensor map expects) and reduce it with one TMA op.
 __device__ __forceinline__ void stage_and_reduce(uint8_t* stg, const CUtensorMap* map, int lane, const uint32_t (&v)[32],
-                                                 int x, int y, int z) {
+                                                 int x, int y, int z, bool store = false) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const uint32_t off = lane * 128 + ((q ^ (lane & 7)) * 16);
@@ -142,7 +150,8 @@ __device__ __forceinline__ void stage_and_reduce(uint8_t* stg, const CUtensorMap
   fence_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_reduce_add_3d(map, stg, x, y, z);
+    if (store) tma_store_3d(map, stg, x, y, z);
+    else tma_reduce_add_3d(map, stg, x, y, z);
     bulk_commit();
   }
 }
@@ -391,11 +400,12 @@ __global__ void __launch_bounds__(448, 1)
           const int row0 = t * C::BQ;
           const int nvalid = sq.len - row0 < C::BQ ? sq.len - row0 : C::BQ;
           float* gdst = p.dq_acc + ((static_cast<size_t>(sq.b) * p.Hq + h) * p.S + sq.start + row0) * DQK;
-          if (dq_mode == kDqBulk) {
+          if (dq_mode == kDqBulk || dq_mode == kDqStore) {  // kDqStore: the same copy, stored
             fence_async_smem();
             named_bar_sync(1, 128);
             if (r == 0) {  // the tile's rows are contiguous in the accumulator: one bulk reduce
-              bulk_reduce_add_f32(gdst, tst, static_cast<uint32_t>(nvalid) * DQK * 4);
+              if (dq_mode == kDqStore) bulk_store_f32(gdst, tst, static_cast<uint32_t>(nvalid) * DQK * 4);
+              else bulk_reduce_add_f32(gdst, tst, static_cast<uint32_t>(nvalid) * DQK * 4);
               bulk_commit();
             }
             ++nbulk;
@@ -421,7 +431,7 @@ __global__ void __launch_bounds__(448, 1)
           continue;
         }
         if constexpr (C::HAS_STAGING) {
-          if (dq_mode == kDqBulk) {
+          if (dq_mode == kDqBulk || dq_mode == kDqStore) {  // kDqStore: same copies, stored
             // the whole row into registers, release the accumulator, then stage and reduce each
             // 32-column chunk through this warp's single staging buffer
             uint32_t v[DQK];
@@ -436,7 +446,7 @@ __global__ void __launch_bounds__(448, 1)
               if (lane == 0 && nbulk >= 1) bulk_wait_read0();  // the previous reduce has read the buffer
               __syncwarp();
               stage_and_reduce(stg, &m.dq_acc, lane, w, 32 * c, sq.start + t * C::BQ + (warp - 8) * 32,
-                               sq.b * p.Hq + h);
+                               sq.b * p.Hq + h, dq_mode == kDqStore);
               ++nbulk;
             }
             continue;

@@ -123,6 +123,12 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* src
                "r"(smem_u32(src)), "r"(bytes)
                : "memory");
 }
+// Bulk copy shared -> global (no reduction); same alignment rules as the reduce.
+__device__ __forceinline__ void bulk_store_f32(float* gdst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

@@ -73,7 +73,10 @@ typedef enum {
   GQA_RED_BULK = 1,    /* cp.reduce.async.bulk ... .add.f32: whole tile rows from shared memory */
   GQA_RED_SCALAR = 2,  /* red.global.add.f32 per element (the slow baseline of [P3]) */
   GQA_RED_NONE = 3     /* BENCHMARK ONLY: partials are stored, not added; dQ (and GROUP_ATOMIC
-                          dK/dV) are WRONG.  Mirrors [P3]'s "entirely omit the atomic_add". */
+                          dK/dV) are WRONG.  Mirrors [P3]'s "entirely omit the atomic_add".
+                          Where the bulk path exists (dQ of the main kernel) the same bulk copies
+                          are issued as stores, so the difference to GQA_RED_BULK is the
+                          reduction alone; elsewhere plain per-thread stores. */
 } gqa_red_mode;
 
 typedef struct {

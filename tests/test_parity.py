@@ -97,11 +97,16 @@ def test_deterministic_bit_identical(name):
             assert torch.equal(a, o[n].view(torch.int16)), n
 
 
-def test_no_accumulation_variant_runs():
-    w = CASES["mha"]
-    inputs, _ = _oracle("mha")
+@pytest.mark.parametrize("case", ["mha", "varlen"])
+def test_no_accumulation_variant_runs(case):
+    """The benchmark-only store mode (d=64 tensor-store and d=128 bulk-store paths): dK / dV are
+    unaffected by the dQ mode and must still match; dQ is only required to be finite."""
+    w = CASES[case]
+    inputs, ref = _oracle(case)
     res = gpu_run(w, inputs, red_mode=nat.GQA_RED_NONE)
-    assert torch.isfinite(res["dk"].float()).all() and torch.isfinite(res["dv"].float()).all()
+    for n in ("dk", "dv"):
+        assert_close(f"{case}:none:{n}", f64(res[n]), ref[n])
+    assert torch.isfinite(res["dq"].float()).all()
 
 
 def test_single_token_and_empty_sequences():
