@@ -176,8 +176,9 @@ gqa_status gqa_attn_fwd(const gqa_attn_params* p, const void* q, const void* k, 
   const bool bf = p->dtype == GQA_BF16;
   Maps m;
   std::memset(&m, 0, sizeof(m));
-  if (!map16(&m.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) || !map16(&m.k, k, p->Dqk, p->S, p->B * p->Hkv, 128, bf) ||
-      !map16(&m.v, v, p->Dv, p->S, p->B * p->Hkv, 128, bf))
+  const int bk = q_kernel_bk();
+  if (!map16(&m.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) || !map16(&m.k, k, p->Dqk, p->S, p->B * p->Hkv, bk, bf) ||
+      !map16(&m.v, v, p->Dv, p->S, p->B * p->Hkv, bk, bf))
     return GQA_ERR_CUDA;
   return to_status(launch_fwd(d.pr, bf, m, sink, o, lse, static_cast<cudaStream_t>(stream)));
 }
@@ -229,9 +230,11 @@ gqa_status gqa_attn_bwd(const gqa_attn_params* p, const void* q, const void* k, 
   cudaError_t e = launch_bwd_kv(d.pr, bf, m, kl, st);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
   if (dq_pass) {
-    Maps m2 = m;
-    if (bq != 128 && (!map16(&m2.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) ||
-                      !map16(&m2.dout, dout, p->Dv, p->S, p->B * p->Hq, 128, bf)))
+    Maps m2 = m;  // the query-stationary pass: 128-row Q / dO boxes, K / V boxes of its key tile
+    const int bk = q_kernel_bk();
+    if (!map16(&m2.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) ||
+        !map16(&m2.dout, dout, p->Dv, p->S, p->B * p->Hq, 128, bf) ||
+        !map16(&m2.k, k, p->Dqk, p->S, p->B * p->Hkv, bk, bf) || !map16(&m2.v, v, p->Dv, p->S, p->B * p->Hkv, bk, bf))
       return GQA_ERR_CUDA;
     e = launch_dq(d.pr, bf, m2, dq, st);
     if (e != cudaSuccess) return GQA_ERR_CUDA;

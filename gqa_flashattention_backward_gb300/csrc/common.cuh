@@ -126,22 +126,22 @@ __host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len, in
   *t1 = b > a ? b : a;
 }
 
-// Key tiles (128 rows) visible to the query tile qt of 128 rows: [*k0, *k1).
-__host__ __device__ __forceinline__ void kv_tiles_for_q_tile(int qt, int len, int causal, int window, int* k0,
+// Key tiles of `bk` rows visible to the query tile qt of 128 rows: [*k0, *k1).
+__host__ __device__ __forceinline__ void kv_tiles_for_q_tile(int qt, int len, int bk, int causal, int window, int* k0,
                                                              int* k1) {
-  const int ntk = (len + 127) / 128;
+  const int ntk = (len + bk - 1) / bk;
   if (!causal) {
     *k0 = 0;
     *k1 = ntk;
     return;
   }
   const int i_lo = qt * 128, i_hi = qt * 128 + 127;
-  int b = i_hi / 128 + 1;
+  int b = i_hi / bk + 1;
   if (b > ntk) b = ntk;
   int a = 0;
   if (window > 0) {
     const int j_lo = i_lo - window + 1;
-    a = j_lo > 0 ? j_lo / 128 : 0;
+    a = j_lo > 0 ? j_lo / bk : 0;
   }
   *k0 = a;
   *k1 = b > a ? b : a;

@@ -35,6 +35,8 @@ cudaError_t launch_selftest_wait(int* err, long long limit, cudaStream_t st);
 cudaError_t launch_fwd(const Problem& p, int dtype_bf16, const Maps& m, const float* sink, void* o, float* lse,
                        cudaStream_t st);
 cudaError_t launch_dq(const Problem& p, int dtype_bf16, const Maps& m, void* dq, cudaStream_t st);
+// Key rows per tile of the query-stationary kernels (the K / V tensor-map box height they need).
+int q_kernel_bk();
 
 // Key/value-stationary backward main kernel.
 cudaError_t launch_bwd_kv(const Problem& p, int dtype_bf16, const Maps& m, const KvLaunch& kl, cudaStream_t st);

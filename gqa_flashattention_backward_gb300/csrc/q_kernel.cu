@@ -1,5 +1,5 @@
 // Query-stationary tcgen05 kernels: one CTA owns 128 query rows of one query
-// head and streams the 128-row key/value tiles it can see.
+// head and streams the 64-row key/value tiles it can see.
 //
 //   FWD : forward with causal / sliding-window / attention-sink masking
 //         (tilelang-ascend PR #1638 "Add GQA Sink Backward BHSD", 4->2 commit:
@@ -7,16 +7,21 @@
 //         over the key tiles: the first forms the row statistics (running max and
 //         sum, sink included), the second forms P = exp(S - LSE) already
 //         normalised and accumulates O = P.V in TMEM, so O is never rescaled.
-//   DQ  : the deterministic dQ pass: S = Q.K^T, dP = dO.V^T, dS = P*(dP - Delta)
-//         (same PR, review thread k1..k5, in the query-stationary loop order the
-//         Ascend kernel uses for dQ, "dQ[L0C accumulate]"); dQ = scale * dS.K
-//         accumulates in TMEM with no atomics.
+//   DQ  : the query-stationary dQ pass (deterministic mode, and the dQ of head
+//         dim 192): S = Q.K^T, dP = dO.V^T, dS = P*(dP - Delta) (same PR, review
+//         thread k1..k5, in the loop order the Ascend kernel uses for dQ,
+//         "dQ[L0C accumulate]"); dQ = scale * dS.K accumulates in TMEM with no
+//         atomics.
 //
-// Warp roles (192 threads): warps 0-3 = softmax warpgroup, thread r owns query
-// row r = TMEM lane r; warp 4 = TMA producer; warp 5 = TMEM allocator + MMA
-// issuer (one elected thread).  Operands live in shared memory in the 128-byte
-// swizzled layout TMA writes; S, dP, O, dQ accumulate in TMEM; P / dS are packed
-// to 16-bit in TMEM and feed the next MMA as its A operand.
+// Warp roles (320 threads): warps 0-3 and 4-7 are two softmax warpgroups that
+// take alternate key tiles (warpgroup w the tiles with index parity w, each with
+// its own TMEM buffer), thread r owns query row r = TMEM lane r; warp 8 = TMA
+// producer; warp 9 = TMEM allocator + MMA issuer (the whole warp runs the loop,
+// one lane elected per MMA).  While one warpgroup works on its tile the tensor
+// core computes the other's, so the softmax and the MMAs overlap.  Operands
+// live in shared memory in the 128-byte swizzled layout TMA writes; S, dP, O,
+// dQ accumulate in TMEM; P / dS are packed to 16 bits in TMEM and feed the next
+// MMA as its A operand.
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include <type_traits>
@@ -28,7 +33,8 @@ namespace gqa {
 
 template <int DQK, int DV, bool FWD>
 struct QCfg {
-  static constexpr int BQ = 128, BK = 128;
+  static constexpr int BQ = 128;  // query rows = TMEM lanes
+  static constexpr int BK = 64;   // keys per tile
   static constexpr int QB = DQK / 64, VB = DV / 64;  // 64-column (128-byte) blocks
   static constexpr int Q_BYTES = BQ * DQK * 2;
   static constexpr int DO_BYTES = FWD ? 0 : BQ * DV * 2;
@@ -37,23 +43,30 @@ struct QCfg {
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
   static constexpr int BUDGET = 220 * 1024;
   static constexpr int KST_RAW = (BUDGET - Q_BYTES - DO_BYTES) / STAGE_BYTES;
-  static constexpr int KST = KST_RAW > 4 ? 4 : (KST_RAW < 1 ? 1 : KST_RAW);
+  static constexpr int KST = KST_RAW > 4 ? 4 : KST_RAW;
   static constexpr int SMEM = 1024 + Q_BYTES + DO_BYTES + KST * STAGE_BYTES;
-  // TMEM columns
-  static constexpr uint32_t T_S0 = 0, T_S1 = 128;         // FWD: two S buffers; DQ: S and dP
-  static constexpr uint32_t T_ACC = 256;                  // FWD: O; DQ: dQ
-  static constexpr int THREADS = 192;
+  // TMEM: warpgroup w's buffer at w*BUF holds S (BK columns; P / dS packed over its first
+  // half) and, for DQ, dP right after it; the accumulator (O or dQ) follows both buffers
+  static constexpr uint32_t BUF = FWD ? BK : 2 * BK;
+  static constexpr uint32_t T_ACC = 2 * BUF;
+  static constexpr uint32_t ACC_COLS = FWD ? DV : DQK;
+  static constexpr uint32_t TMEM_COLS = (T_ACC + ACC_COLS <= 256) ? 256 : 512;
+  static constexpr int THREADS = 320;
+  static_assert(KST >= 2, "stages");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(T_ACC + (FWD ? DV : DQK) <= 512, "tmem");
+  static_assert(T_ACC + ACC_COLS <= 512, "tmem");
+  static_assert(ACC_COLS % 64 == 0, "each warpgroup drains whole 32-column chunks");
 };
 
 struct QSmemCtl {
   uint64_t bar_q;
   uint64_t kv_full[4], kv_empty[4];
-  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t s_full[2];   // tensor core -> warpgroup w: S (and dP) of its tile are in TMEM
+  uint64_t sm_done[2];  // warpgroup w -> tensor core: S read / P or dS stored, buffer reusable
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort_flag;
+  float stat_m[2][128], stat_l[2][128];  // FWD: each warpgroup's row statistics, combined once
 };
 
 // Allowed-key test for query row i (local) and key j (local).
@@ -62,7 +75,7 @@ __device__ __forceinline__ bool allowed(int i, int j, int len, int causal, int w
 }
 
 template <int DQK, int DV, bool BF16, bool FWD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     q_kernel(const Problem p, const __grid_constant__ Maps m, const float* __restrict__ sink, void* __restrict__ out,
              float* __restrict__ lse_out) {
   using C = QCfg<DQK, DV, FWD>;
@@ -82,7 +95,7 @@ __global__ void __launch_bounds__(192, 1)
   const int t = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tiles first
   if (t >= ntq) return;
   int k0, k1;
-  kv_tiles_for_q_tile(t, sq.len, p.causal, p.window, &k0, &k1);
+  kv_tiles_for_q_tile(t, sq.len, C::BK, p.causal, p.window, &k0, &k1);
   const int n = k1 - k0;
   const int NIT = FWD ? 2 * n : n;
   const int g = h / p.G;
@@ -100,26 +113,24 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.s_free[i], 4);  // one arrival per softmax warp
-      mbar_init(&ctl.p_full[i], 4);
+      mbar_init(&ctl.sm_done[i], 4);  // one arrival per warp of the warpgroup
     }
     mbar_init(&ctl.acc_done, 1);
     ctl.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(&ctl.tmem_base, 512);
+  if (warp == 9) {
+    tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // broadcast from lane 0 so the compiler treats the TMEM base as warp-uniform (uniform registers
-  // for the MMA operands instead of per-MMA register moves)
+  // broadcast from lane 0 so the compiler treats the TMEM base as warp-uniform
   const uint32_t tmem = __shfl_sync(0xffffffffu, ctl.tmem_base, 0);
   const WaitGuard guard{p.err, &ctl.abort_flag, p.wait_limit};
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_map(&m.q);
@@ -156,161 +167,183 @@ __global__ void __launch_bounds__(192, 1)
           mbar_wait(&ctl.kv_full[it % C::KST], (it / C::KST) & 1, g2, 0);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     {  // the whole warp runs the issue loop; one elected lane issues each MMA
       constexpr uint32_t idS = idesc_f16(128, C::BK, BF16, false, false);
       constexpr uint32_t idPV = idesc_f16(128, DV, BF16, false, true);
       constexpr uint32_t idDQ = idesc_f16(128, DQK, BF16, false, true);
-      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);    // Q, K-major (A of S)
+      const uint64_t dDO0 = sdesc_sw128(smem_u32(sDO), 16, 1024);  // dO, K-major (A of dP)
+      auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
       bool ok = mbar_wait_warp(&ctl.bar_q, 0, guard, 2);
-      int pending = -1;  // output-pass tile whose P.V is not issued yet
-      auto issue_pv = [&](int j) -> bool {
-        const int u = j - n;
-        if (!mbar_wait_warp(&ctl.p_full[u & 1], (u >> 1) & 1, guard, 5)) return false;
+      // S (and dP) of tile `it` into warpgroup (it & 1)'s buffer
+      auto issue_s = [&](int it) -> bool {
+        const int st = it % C::KST, w = it & 1;
+        if (!mbar_wait_warp(&ctl.kv_full[st], (it / C::KST) & 1, guard, 3)) return false;
+        if (it >= 2 && !mbar_wait_warp(&ctl.sm_done[w], ((it - 2) >> 1) & 1, guard, 4)) return false;
         tc_fence_after();
-        const uint32_t tP = tmem + ((j & 1) ? C::T_S1 : C::T_S0);
-        const uint32_t aVj = smem_u32(sK0 + (j % C::KST) * C::STAGE_BYTES) + C::K_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)
-          umma_ts(tmem + C::T_ACC, tP + kk * 8, sdesc_sw128(aVj + kk * 2048, C::BK * 128, 1024), idPV,
-                  (u > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&ctl.kv_empty[j % C::KST]);
-        return true;
-      };
-      for (int it = 0; ok && it < NIT; ++it) {
-        const int st = it % C::KST;
         const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
-        const uint32_t aV = aK + C::K_BYTES;
-        if (!mbar_wait_warp(&ctl.kv_full[st], (it / C::KST) & 1, guard, 3)) break;
-        if (FWD) {
-          const int buf = it & 1;
-          if (it >= 2 && !mbar_wait_warp(&ctl.s_free[buf], ((it - 2) >> 1) & 1, guard, 4)) break;
-          tc_fence_after();
-          const uint32_t tS = tmem + (buf ? C::T_S1 : C::T_S0);
+        const uint64_t dK = sdesc_sw128(aK, 16, 1024);
+        const uint32_t tS = tmem + w * C::BUF;
 #pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk)
-            umma_ss(tS, sdesc_sw128(aQ + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024),
-                    sdesc_sw128(aK + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
-          umma_commit(&ctl.s_full[buf]);
-          if (it < n) umma_commit(&ctl.kv_empty[st]);  // statistics pass: K consumed by S alone
-          // the P.V of the previous output-pass tile goes after this tile's S (one tile of lookahead)
-          if (pending >= 0) {
-            if (!issue_pv(pending)) break;
-            pending = -1;
-          }
-          if (it >= n) pending = it;
-        } else {
-          if (it >= 1 && !mbar_wait_warp(&ctl.s_free[0], (it - 1) & 1, guard, 4)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk)
-            umma_ss(tmem + C::T_S0, sdesc_sw128(aQ + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024),
-                    sdesc_sw128(aK + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
+        for (int kk = 0; kk < DQK / 16; ++kk)
+          umma_ss(tS, desc_advance(dQ0, kstep(kk, C::BQ)), desc_advance(dK, kstep(kk, C::BK)), idS, kk > 0);
+        if (!FWD) {
+          const uint64_t dV = sdesc_sw128(aK + C::K_BYTES, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk)
-            umma_ss(tmem + C::T_S1, sdesc_sw128(aDO + (kk / 4) * (C::BQ * 128) + (kk % 4) * 32, 16, 1024),
-                    sdesc_sw128(aV + (kk / 4) * (C::BK * 128) + (kk % 4) * 32, 16, 1024), idS, kk > 0);
-          umma_commit(&ctl.s_full[0]);
-          if (!mbar_wait_warp(&ctl.p_full[0], it & 1, guard, 5)) break;
-          tc_fence_after();
+            umma_ss(tS + C::BK, desc_advance(dDO0, kstep(kk, C::BQ)), desc_advance(dV, kstep(kk, C::BK)), idS,
+                    kk > 0);
+        }
+        umma_commit(&ctl.s_full[w]);
+        if (FWD && it < n) umma_commit(&ctl.kv_empty[st]);  // statistics pass: K consumed by S alone
+        return true;
+      };
+      // FWD: O += P.V; DQ: dQ += dS.K -- A = the packed P / dS in the warpgroup's buffer
+      auto issue_acc = [&](int it) -> bool {
+        const int st = it % C::KST, w = it & 1;
+        if (!mbar_wait_warp(&ctl.sm_done[w], (it >> 1) & 1, guard, 5)) return false;
+        tc_fence_after();
+        const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
+        const uint32_t tA = tmem + w * C::BUF;
+        const int first = FWD ? n : 0;
+        if (FWD) {
+          const uint64_t dVmn = sdesc_sw128(aK + C::K_BYTES, C::BK * 128, 1024);  // V, MN-major (B of P.V)
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
-            umma_ts(tmem + C::T_ACC, tmem + C::T_S1 + kk * 8, sdesc_sw128(aK + kk * 2048, C::BK * 128, 1024),
-                    idDQ, (it > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&ctl.kv_empty[st]);
+            umma_ts(tmem + C::T_ACC, tA + kk * 8, desc_advance(dVmn, kk * 2048), idPV,
+                    (it > first || kk > 0) ? 1u : 0u);
+        } else {
+          const uint64_t dKmn = sdesc_sw128(aK, C::BK * 128, 1024);  // K, MN-major (B of dS.K)
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk)
+            umma_ts(tmem + C::T_ACC, tA + kk * 8, desc_advance(dKmn, kk * 2048), idDQ,
+                    (it > first || kk > 0) ? 1u : 0u);
         }
+        umma_commit(&ctl.kv_empty[st]);
+        return true;
+      };
+      if (ok && NIT > 0) ok = issue_s(0);
+      if (ok && NIT > 1) ok = issue_s(1);
+      for (int it = 0; ok && it < NIT; ++it) {
+        if ((!FWD || it >= n) && !issue_acc(it)) break;
+        if (it + 2 < NIT && !issue_s(it + 2)) break;
       }
-      if (FWD && ok && pending >= 0) issue_pv(pending);
       umma_commit(&ctl.acc_done);
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int r = tid;  // query row within the tile == TMEM lane
+    // ------------------------------------------------------------ softmax warpgroups
+    const int w = warp >> 2;  // which tiles: index parity w
+    const int r = tid & 127;  // query row within the tile == TMEM lane
     const int il = t * C::BQ + r;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + w * C::BUF;
     const float sl2 = p.scale_log2;
+    const float2 sl22 = make_float2(sl2, sl2);
     bool ok = true;
     if (FWD) {
-      float mx = -INFINITY, l = 0.f;  // running max (log2 units) and sum
-      if (sink) {
+      float mx = -INFINITY, l = 0.f;  // running max (log2 units) and sum of this warpgroup's tiles
+      if (sink && w == 0) {
         mx = __ldg(sink + h) * kLog2e;
         l = 1.f;
       }
-      float lse2 = 0.f;
-      for (int it = 0; it < NIT; ++it) {
-        const int buf = it & 1;
+      float lse2 = INFINITY;
+      bool combined = false;
+      // both warpgroups' statistics -> LSE2 of the row (once, before the first output tile)
+      auto combine = [&]() {
+        ctl.stat_m[w][r] = mx;
+        ctl.stat_l[w][r] = l;
+        named_bar_sync(1, 256);
+        const float m0 = ctl.stat_m[0][r], m1 = ctl.stat_m[1][r];
+        const float M = fmaxf(m0, m1);
+        float L = 0.f;
+        if (M != -INFINITY) {
+          if (m0 != -INFINITY) L += ctl.stat_l[0][r] * ex2_approx(m0 - M);
+          if (m1 != -INFINITY) L += ctl.stat_l[1][r] * ex2_approx(m1 - M);
+        }
+        lse2 = (L > 0.f) ? M + log2f(L) : INFINITY;
+        combined = true;
+      };
+      for (int it = w, k = 0; it < NIT; it += 2, ++k) {
         const int kt = k0 + it % n;
         const int j0 = kt * C::BK;
         const bool need_mask = (j0 + C::BK > sq.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ) ||
                                (p.window > 0 && t * C::BQ + C::BQ - 1 - j0 >= p.window);
-        if (!mbar_wait_warp(&ctl.s_full[buf], (it >> 1) & 1, guard, 6)) {
+        if (it >= n && !combined) combine();
+        if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t tS = tmem + lane_base + (buf ? C::T_S1 : C::T_S0);
+        uint32_t v[C::BK];
+        tmem_ld64(tS, v);
         if (it < n) {
           // statistics pass
-#pragma unroll 1
-          for (int c0 = 0; c0 < C::BK; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tS + c0, v);
-            float cm = -INFINITY;
+          float cm = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float x = __uint_as_float(v[e]) * sl2;
-              if (need_mask && !allowed(il, j0 + c0 + e, sq.len, p.causal, p.window)) x = -INFINITY;
-              v[e] = __float_as_uint(x);
-              cm = fmaxf(cm, x);
-            }
-            const float mn = fmaxf(mx, cm);
-            if (mn != -INFINITY) {
-              float acc = 0.f;
+          for (int e = 0; e < C::BK; ++e) {
+            float x = __uint_as_float(v[e]) * sl2;
+            if (need_mask && !allowed(il, j0 + e, sq.len, p.causal, p.window)) x = -INFINITY;
+            v[e] = __float_as_uint(x);
+            cm = fmaxf(cm, x);
+          }
+          const float mn = fmaxf(mx, cm);
+          if (mn != -INFINITY) {
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) acc += ex2_approx(__uint_as_float(v[e]) - mn);
-              l = l * ex2_approx(mx - mn) + acc;
-              mx = mn;
+            for (int e = 0; e < C::BK; e += 2) {
+              a0 += ex2_approx(__uint_as_float(v[e]) - mn);
+              a1 += ex2_approx(__uint_as_float(v[e + 1]) - mn);
             }
+            l = l * ex2_approx(mx - mn) + (a0 + a1);
+            mx = mn;
           }
           tc_fence_before();
-          mbar_arrive_warp(&ctl.s_free[buf]);
-          if (it == n - 1) lse2 = (l > 0.f) ? mx + log2f(l) : INFINITY;
         } else {
           // output pass: P = exp2(S*scale*log2e - LSE2), packed in place over S
-          const int u = it - n;
-#pragma unroll 1
-          for (int c0 = 0; c0 < C::BK; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tS + c0, v);
-            uint32_t pk[16];
+          uint32_t pk[C::BK / 2];
+          const float2 nl = make_float2(-lse2, -lse2);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float a = ex2_approx(fmaf(__uint_as_float(v[2 * e]), sl2, -lse2));
-              float b = ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -lse2));
-              if (need_mask) {
-                if (!allowed(il, j0 + c0 + 2 * e, sq.len, p.causal, p.window)) a = 0.f;
-                if (!allowed(il, j0 + c0 + 2 * e + 1, sq.len, p.causal, p.window)) b = 0.f;
-              }
-              pk[e] = pack2<BF16>(a, b);
+          for (int e = 0; e < C::BK; e += 4) {
+            const float2 x0 = fma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl22, nl);
+            const float2 x1 = fma2(make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), sl22, nl);
+            if (BF16) {
+              pk[e / 2] = pack2<true>(ex2_approx(x0.x), ex2_approx(x0.y));
+              pk[e / 2 + 1] = pack2<true>(ex2_approx(x1.x), ex2_approx(x1.y));
+            } else {
+              // the argument rounded to fp16, exponentiated two at a time (adds at most ~2e-4 to P)
+              pk[e / 2] = ex2_f16x2(pack2<false>(x0.x, x0.y));
+              pk[e / 2 + 1] = ex2_f16x2(pack2<false>(x1.x, x1.y));
             }
-            tmem_st16(tS + c0 / 2, pk);
           }
+          if (need_mask) {
+#pragma unroll
+            for (int e = 0; e < C::BK; ++e)
+              if (!allowed(il, j0 + e, sq.len, p.causal, p.window)) pk[e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+          }
+          uint32_t p0[16], p1[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            p0[e] = pk[e];
+            p1[e] = pk[16 + e];
+          }
+          tmem_st16(tS, p0);
+          tmem_st16(tS + 16, p1);
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive_warp(&ctl.p_full[u & 1]);
-          mbar_arrive_warp(&ctl.s_free[buf]);
         }
+        mbar_arrive_warp(&ctl.sm_done[w]);
       }
-      if (n == 0) lse2 = (l > 0.f) ? mx + log2f(l) : INFINITY;
-      // epilogue: O (already normalised) and LSE
+      if (!combined) combine();  // both warpgroups reach the named barrier exactly once
+      // epilogue: O (already normalised) and LSE; warpgroup w writes output columns [w*DV/2, (w+1)*DV/2)
       if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
         tc_fence_after();
         const bool valid = il < sq.len;
         const size_t orow = (static_cast<size_t>(zq) * p.S + sq.start + il);
         T* o = static_cast<T*>(out) + orow * DV;
 #pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
+        for (int c0 = w * (DV / 2); c0 < (w + 1) * (DV / 2); c0 += 32) {
           uint32_t v[32];
           if (n > 0) tmem_ld32(tmem + lane_base + C::T_ACC + c0, v);
           else
@@ -318,38 +351,37 @@ __global__ void __launch_bounds__(192, 1)
           if (valid) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1]));
-              w.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
-              w.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
-              w.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
-              *reinterpret_cast<uint4*>(o + c0 + 8 * q4) = w;
+              uint4 u;
+              u.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1]));
+              u.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
+              u.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
+              u.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
+              *reinterpret_cast<uint4*>(o + c0 + 8 * q4) = u;
             }
           }
         }
-        if (valid) lse_out[orow] = lse2 * kLn2;
+        if (valid && w == 0) lse_out[orow] = lse2 * kLn2;
       }
     } else {
-      // deterministic dQ pass
+      // query-stationary dQ pass
       const size_t sidx = stat_index(p, h, s, t) + r;
       const float nlse2 = p.nlse2[sidx];
       const float ndlt = p.ndelta[sidx];
-      for (int it = 0; it < NIT; ++it) {
+      for (int it = w, k = 0; it < NIT; it += 2, ++k) {
         const int kt = k0 + it;
         const int j0 = kt * C::BK;
         const bool need_mask = (j0 + C::BK > sq.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ) ||
                                (p.window > 0 && t * C::BQ + C::BQ - 1 - j0 >= p.window);
-        if (!mbar_wait_warp(&ctl.s_full[0], it & 1, guard, 6)) {
+        if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t tS = tmem + lane_base + C::T_S0, tP = tmem + lane_base + C::T_S1;
-#pragma unroll 1
+#pragma unroll
         for (int c0 = 0; c0 < C::BK; c0 += 32) {
           uint32_t sv[32], dv[32];
           tmem_ld32(tS + c0, sv);
-          tmem_ld32(tP + c0, dv);
+          tmem_ld32(tS + C::BK + c0, dv);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -363,33 +395,34 @@ __global__ void __launch_bounds__(192, 1)
             const float db = pb * (__uint_as_float(dv[2 * e + 1]) + ndlt);
             pk[e] = pack2<BF16>(da, db);
           }
-          tmem_st16(tP + c0 / 2, pk);
+          // dS packed over S's first half: chunk c0 lands in columns [c0/2, c0/2 + 16), already read
+          tmem_st16(tS + c0 / 2, pk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive_warp(&ctl.p_full[0]);
-        mbar_arrive_warp(&ctl.s_free[0]);
+        mbar_arrive_warp(&ctl.sm_done[w]);
       }
+      // epilogue: dQ (x scale); warpgroup w writes columns [w*DQK/2, (w+1)*DQK/2)
       if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
         tc_fence_after();
         const bool valid = il < sq.len;
         const size_t qrow = static_cast<size_t>(zq) * p.S + sq.start + il;
         T* dq = static_cast<T*>(out) + qrow * DQK;
-        if (n > 0) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < DQK; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + C::T_ACC + c0, v);  // all lanes: .sync.aligned
-            if (!valid) continue;
+        for (int c0 = w * (DQK / 2); c0 < (w + 1) * (DQK / 2); c0 += 32) {
+          uint32_t v[32];
+          if (n > 0) tmem_ld32(tmem + lane_base + C::T_ACC + c0, v);  // all lanes: .sync.aligned
+          else
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          if (!valid) continue;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]) * p.scale, __uint_as_float(v[8 * q4 + 1]) * p.scale);
-              w.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]) * p.scale, __uint_as_float(v[8 * q4 + 3]) * p.scale);
-              w.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]) * p.scale, __uint_as_float(v[8 * q4 + 5]) * p.scale);
-              w.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]) * p.scale, __uint_as_float(v[8 * q4 + 7]) * p.scale);
-              *reinterpret_cast<uint4*>(dq + c0 + 8 * q4) = w;
-            }
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 u;
+            u.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]) * p.scale, __uint_as_float(v[8 * q4 + 1]) * p.scale);
+            u.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]) * p.scale, __uint_as_float(v[8 * q4 + 3]) * p.scale);
+            u.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]) * p.scale, __uint_as_float(v[8 * q4 + 5]) * p.scale);
+            u.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]) * p.scale, __uint_as_float(v[8 * q4 + 7]) * p.scale);
+            *reinterpret_cast<uint4*>(dq + c0 + 8 * q4) = u;
           }
         }
       }
@@ -398,9 +431,9 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -440,5 +473,7 @@ cudaError_t launch_fwd(const Problem& p, int dtype_bf16, const Maps& m, const fl
 cudaError_t launch_dq(const Problem& p, int dtype_bf16, const Maps& m, void* dq, cudaStream_t st) {
   return dispatch_q<false>(p, dtype_bf16, m, nullptr, dq, nullptr, st);
 }
+
+int q_kernel_bk() { return QCfg<64, 64, true>::BK; }
 
 }  // namespace gqa
