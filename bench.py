@@ -313,6 +313,32 @@ def run_gpu(args):
                                     frac_of_peak_exact=round(wc.flops_exact() / (stp * 1e-3) / 1e12 / peaks["bf16_tflops"], 4))
             del cc
 
+    # the forward (prerequisite of the backward, not part of the step): exact-count TFLOP/s per workload
+    forward = {}
+    if not args.no_forward:
+        for wf in (w, W.varlen(), W.sink_window(), W.long_context()):
+            cf = c if wf is w else setup(wf)
+            nst = max(3, args.steps // 2)
+
+            def fstep():
+                nat.fwd(cf["p"], cf["q"], cf["k"], cf["v"], cf["sink"], cf["o"], cf["lse"], cf["ws"])
+
+            for _ in range(args.warmup):
+                fstep()
+            torch.cuda.synchronize()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record()
+            for _ in range(nst):
+                fstep()
+            f1.record()
+            torch.cuda.synchronize()
+            fms = f0.elapsed_time(f1) / nst
+            fflops = 2.0 * wf.pairs() * (wf.Dqk + wf.Dv)
+            forward[wf.name] = dict(ms=round(fms, 4), tflops_exact=round(fflops / (fms * 1e-3) / 1e12, 2),
+                                    frac_of_peak_exact=round(fflops / (fms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4))
+            if cf is not c:
+                del cf
+
     line = None
     if rank == 0:
         cpu = None
@@ -330,7 +356,7 @@ def run_gpu(args):
                     flops_per_step_convention=flops_conv, flops_per_step_exact=flops_exact,
                     frac_of_peak_exact=round(flops_exact / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clocks,
-                    variants=variants, sweep=sweep, configs=configs)
+                    variants=variants, sweep=sweep, configs=configs, forward=forward)
         print(json.dumps(line), flush=True)
     if ws_n > 1:
         dist.barrier()
@@ -414,6 +440,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--no-forward", action="store_true", help="skip the forward timings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

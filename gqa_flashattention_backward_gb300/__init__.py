@@ -8,6 +8,8 @@ the C ABI prescribes:
 * :func:`attention_forward`  -> ``gqa_attn_fwd``
 * :func:`attention_backward` -> ``gqa_attn_bwd_preprocess``, ``gqa_attn_bwd``,
   ``gqa_attn_bwd_postprocess`` and (with a sink) ``gqa_attn_dsink``.
+* :func:`gqa_attention` -> both, as a ``torch.autograd.Function`` (O from the
+  forward, dQ / dK / dV / dsink from the backward when autograd asks for them).
 
 Tensors use the BHSD layout: q [B,Hq,S,Dqk], k [B,Hkv,S,Dqk], v [B,Hkv,S,Dv],
 o/dout [B,Hq,S,Dv]; packed variable-length batches use B=1 and ``cu_seqlens``.
@@ -23,7 +25,7 @@ from ._native import (GQA_GROUP_ATOMIC, GQA_GROUP_TMEM, GQA_RED_BULK, GQA_RED_NO
                       GQA_RED_V4, GqaError)
 
 __all__ = [
-    "attention_forward", "attention_backward", "preferred_red_mode", "native", "GqaError", "GQA_GROUP_TMEM", "GQA_GROUP_ATOMIC",
+    "attention_forward", "attention_backward", "gqa_attention", "GqaAttentionFunction", "preferred_red_mode", "native", "GqaError", "GQA_GROUP_TMEM", "GQA_GROUP_ATOMIC",
     "GQA_RED_V4", "GQA_RED_BULK", "GQA_RED_SCALAR", "GQA_RED_NONE",
 ]
 
@@ -92,3 +94,33 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
     if sink is not None:
         native.dsink(p, sink, lse, res["delta"], res["dsink"])
     return res
+
+
+class GqaAttentionFunction(torch.autograd.Function):
+    """Autograd wrapper: the forward saves Q, K, V, O and LSE; the backward runs the four
+    backward entry points on them.  Every step runs in the CUDA library."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic):
+        o, lse = attention_forward(q, k, v, causal=causal, window=window, scale=scale, sink=sink,
+                                   cu_seqlens=cu_seqlens, max_seqlen=max_seqlen)
+        ctx.save_for_backward(q, k, v, o, lse, sink)
+        ctx.opts = dict(causal=causal, window=window, scale=scale, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
+                        deterministic=deterministic)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, sink = ctx.saved_tensors
+        g = attention_backward(q, k, v, o, lse, do.contiguous(), sink=sink, **ctx.opts)
+        dsink = g.get("dsink") if sink is not None and ctx.needs_input_grad[3] else None
+        return g["dq"], g["dk"], g["dv"], dsink, None, None, None, None, None, None
+
+
+def gqa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = True, window: int = 0,
+                  scale: Optional[float] = None, sink: Optional[torch.Tensor] = None,
+                  cu_seqlens: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
+                  deterministic: bool = False) -> torch.Tensor:
+    """Differentiable grouped-query attention: returns O [B,Hq,S,Dv]; ``O.backward(dO)`` fills
+    q.grad, k.grad, v.grad (and sink.grad, fp32) through the backward kernels."""
+    return GqaAttentionFunction.apply(q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic)

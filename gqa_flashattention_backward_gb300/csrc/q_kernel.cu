@@ -4,9 +4,10 @@
 //   FWD : forward with causal / sliding-window / attention-sink masking
 //         (tilelang-ascend PR #1638 "Add GQA Sink Backward BHSD", 4->2 commit:
 //         "flashattn_fwd: online softmax + sink + window -> O, lse").  Two passes
-//         over the key tiles: the first forms the row statistics (running max and
-//         sum, sink included), the second forms P = exp(S - LSE) already
-//         normalised and accumulates O = P.V in TMEM, so O is never rescaled.
+//         over the key tiles: the first finds each row's maximum logit (sink
+//         included; no exponentials), the second forms P = exp(S - max) <= 1 and
+//         accumulates P.[V | 1] in TMEM, whose extra column is the row sum l, so
+//         O = (P.V) / l and LSE = max + log l with no rescaling of O.
 //   DQ  : the query-stationary dQ pass (deterministic mode, and the dQ of head
 //         dim 192): S = Q.K^T, dP = dO.V^T, dS = P*(dP - Delta) (same PR, review
 //         thread k1..k5, in the loop order the Ascend kernel uses for dQ,
@@ -40,7 +41,9 @@ struct QCfg {
   static constexpr int DO_BYTES = FWD ? 0 : BQ * DV * 2;
   static constexpr int K_BYTES = BK * DQK * 2;
   static constexpr int V_BYTES = BK * DV * 2;
-  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
+  // FWD: a 64-column block of ones after V in every stage, so P.[V | 1] also yields sum_j P
+  static constexpr int ONES_BYTES = FWD ? BK * 128 : 0;
+  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES + ONES_BYTES;
   static constexpr int BUDGET = 220 * 1024;
   static constexpr int KST_RAW = (BUDGET - Q_BYTES - DO_BYTES) / STAGE_BYTES;
   static constexpr int KST = KST_RAW > 4 ? 4 : KST_RAW;
@@ -49,13 +52,14 @@ struct QCfg {
   // half) and, for DQ, dP right after it; the accumulator (O or dQ) follows both buffers
   static constexpr uint32_t BUF = FWD ? BK : 2 * BK;
   static constexpr uint32_t T_ACC = 2 * BUF;
-  static constexpr uint32_t ACC_COLS = FWD ? DV : DQK;
+  static constexpr uint32_t ACC_COLS = FWD ? DV + 16 : DQK;  // FWD: O and 16 columns of the row sum
+  static constexpr uint32_t OUT_COLS = FWD ? DV : DQK;       // columns written out
   static constexpr uint32_t TMEM_COLS = (T_ACC + ACC_COLS <= 256) ? 256 : 512;
   static constexpr int THREADS = 320;
   static_assert(KST >= 2, "stages");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(T_ACC + ACC_COLS <= 512, "tmem");
-  static_assert(ACC_COLS % 64 == 0, "each warpgroup drains whole 32-column chunks");
+  static_assert(OUT_COLS % 64 == 0, "each warpgroup drains whole 32-column chunks");
 };
 
 struct QSmemCtl {
@@ -66,7 +70,7 @@ struct QSmemCtl {
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort_flag;
-  float stat_m[2][128], stat_l[2][128];  // FWD: each warpgroup's row statistics, combined once
+  float stat_m[2][128];  // FWD: each warpgroup's row maxima, combined once
 };
 
 // Allowed-key test for query row i (local) and key j (local).
@@ -123,6 +127,15 @@ __global__ void __launch_bounds__(320, 1)
     tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
+  if (FWD) {
+    // the constant ones blocks (TMA never writes them); 1.0 in the input dtype
+    const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
+    for (int st = 0; st < C::KST; ++st) {
+      uint4* blk = reinterpret_cast<uint4*>(sK0 + st * C::STAGE_BYTES + C::K_BYTES + C::V_BYTES);
+      for (int i = tid; i < C::ONES_BYTES / 16; i += C::THREADS) blk[i] = make_uint4(one2, one2, one2, one2);
+    }
+    fence_async_smem();  // generic-proxy writes read later by the tensor core
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -171,7 +184,7 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ MMA issuer
     {  // the whole warp runs the issue loop; one elected lane issues each MMA
       constexpr uint32_t idS = idesc_f16(128, C::BK, BF16, false, false);
-      constexpr uint32_t idPV = idesc_f16(128, DV, BF16, false, true);
+      constexpr uint32_t idPV = idesc_f16(128, DV + 16, BF16, false, true);  // P.[V | 1]
       constexpr uint32_t idDQ = idesc_f16(128, DQK, BF16, false, true);
       const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);    // Q, K-major (A of S)
       const uint64_t dDO0 = sdesc_sw128(smem_u32(sDO), 16, 1024);  // dO, K-major (A of dP)
@@ -209,7 +222,8 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t tA = tmem + w * C::BUF;
         const int first = FWD ? n : 0;
         if (FWD) {
-          const uint64_t dVmn = sdesc_sw128(aK + C::K_BYTES, C::BK * 128, 1024);  // V, MN-major (B of P.V)
+          // [V | ones], MN-major (B of P.[V | 1]): the ones block follows V's 64-column blocks
+          const uint64_t dVmn = sdesc_sw128(aK + C::K_BYTES, C::BK * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
             umma_ts(tmem + C::T_ACC, tA + kk * 8, desc_advance(dVmn, kk * 2048), idPV,
@@ -243,26 +257,17 @@ __global__ void __launch_bounds__(320, 1)
     const float2 sl22 = make_float2(sl2, sl2);
     bool ok = true;
     if (FWD) {
-      float mx = -INFINITY, l = 0.f;  // running max (log2 units) and sum of this warpgroup's tiles
-      if (sink && w == 0) {
-        mx = __ldg(sink + h) * kLog2e;
-        l = 1.f;
-      }
-      float lse2 = INFINITY;
+      float mx = -INFINITY;  // running maximum of this warpgroup's logits (log2 units)
+      const float sink2 = sink ? __ldg(sink + h) * kLog2e : -INFINITY;
+      if (w == 0) mx = sink2;
+      float mref = 0.f;  // the row maximum both passes agree on (0 for a row with no allowed key)
       bool combined = false;
-      // both warpgroups' statistics -> LSE2 of the row (once, before the first output tile)
+      // both warpgroups' maxima -> the row maximum (once, before the first output tile)
       auto combine = [&]() {
         ctl.stat_m[w][r] = mx;
-        ctl.stat_l[w][r] = l;
         named_bar_sync(1, 256);
-        const float m0 = ctl.stat_m[0][r], m1 = ctl.stat_m[1][r];
-        const float M = fmaxf(m0, m1);
-        float L = 0.f;
-        if (M != -INFINITY) {
-          if (m0 != -INFINITY) L += ctl.stat_l[0][r] * ex2_approx(m0 - M);
-          if (m1 != -INFINITY) L += ctl.stat_l[1][r] * ex2_approx(m1 - M);
-        }
-        lse2 = (L > 0.f) ? M + log2f(L) : INFINITY;
+        const float M = fmaxf(ctl.stat_m[0][r], ctl.stat_m[1][r]);
+        mref = (M == -INFINITY) ? 0.f : M;
         combined = true;
       };
       for (int it = w, k = 0; it < NIT; it += 2, ++k) {
@@ -279,31 +284,24 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t v[C::BK];
         tmem_ld64(tS, v);
         if (it < n) {
-          // statistics pass
-          float cm = -INFINITY;
+          // first pass: the row maximum of the raw logits (scale > 0 commutes with max)
+          float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < C::BK; ++e) {
-            float x = __uint_as_float(v[e]) * sl2;
-            if (need_mask && !allowed(il, j0 + e, sq.len, p.causal, p.window)) x = -INFINITY;
-            v[e] = __float_as_uint(x);
-            cm = fmaxf(cm, x);
-          }
-          const float mn = fmaxf(mx, cm);
-          if (mn != -INFINITY) {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < C::BK; e += 2) {
-              a0 += ex2_approx(__uint_as_float(v[e]) - mn);
-              a1 += ex2_approx(__uint_as_float(v[e + 1]) - mn);
+          for (int e = 0; e < C::BK; e += 2) {
+            float a = __uint_as_float(v[e]), b = __uint_as_float(v[e + 1]);
+            if (need_mask) {
+              if (!allowed(il, j0 + e, sq.len, p.causal, p.window)) a = -INFINITY;
+              if (!allowed(il, j0 + e + 1, sq.len, p.causal, p.window)) b = -INFINITY;
             }
-            l = l * ex2_approx(mx - mn) + (a0 + a1);
-            mx = mn;
+            c0 = fmaxf(c0, a);
+            c1 = fmaxf(c1, b);
           }
+          mx = fmaxf(mx, fmaxf(c0, c1) * sl2);
           tc_fence_before();
         } else {
-          // output pass: P = exp2(S*scale*log2e - LSE2), packed in place over S
+          // second pass: P = exp2(S*scale*log2e - max) <= 1, packed in place over S
           uint32_t pk[C::BK / 2];
-          const float2 nl = make_float2(-lse2, -lse2);
+          const float2 nl = make_float2(-mref, -mref);
 #pragma unroll
           for (int e = 0; e < C::BK; e += 4) {
             const float2 x0 = fma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl22, nl);
@@ -336,11 +334,20 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive_warp(&ctl.sm_done[w]);
       }
       if (!combined) combine();  // both warpgroups reach the named barrier exactly once
-      // epilogue: O (already normalised) and LSE; warpgroup w writes output columns [w*DV/2, (w+1)*DV/2)
+      // epilogue: l = sum_j P (the ones column) + the sink's term; O = (P.V) / l; LSE = max + log l.
+      // warpgroup w writes output columns [w*DV/2, (w+1)*DV/2)
       if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
         tc_fence_after();
         const bool valid = il < sq.len;
         const size_t orow = (static_cast<size_t>(zq) * p.S + sq.start + il);
+        float l = 0.f;
+        if (n > 0) {
+          uint32_t sv[16];
+          tmem_ld16(tmem + lane_base + C::T_ACC + DV, sv);
+          l = __uint_as_float(sv[0]);
+        }
+        if (sink2 != -INFINITY) l += ex2_approx(sink2 - mref);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
         T* o = static_cast<T*>(out) + orow * DV;
 #pragma unroll 1
         for (int c0 = w * (DV / 2); c0 < (w + 1) * (DV / 2); c0 += 32) {
@@ -352,15 +359,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 u;
-              u.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1]));
-              u.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
-              u.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
-              u.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
+              u.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+              u.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+              u.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+              u.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
               *reinterpret_cast<uint4*>(o + c0 + 8 * q4) = u;
             }
           }
         }
-        if (valid && w == 0) lse_out[orow] = lse2 * kLn2;
+        if (valid && w == 0) lse_out[orow] = (l > 0.f) ? (mref + log2f(l)) * kLn2 : -INFINITY;
       }
     } else {
       // query-stationary dQ pass
