@@ -15,6 +15,7 @@ namespace gqa {
 bool kv_kernel_has_dq(int Dqk);
 bool kv_kernel_has_bulk_dq(int Dqk);
 int kv_kernel_bq(int Dqk);
+bool kv_kernel_folds_stats(int Dqk);
 }  // namespace gqa
 
 using namespace gqa;
@@ -85,7 +86,7 @@ gqa_status validate(const gqa_attn_params* p) {
 struct Derived {
   Problem pr;
   WsLayout ws;
-  bool need_dq_acc, need_dkdv_acc, group_tmem;
+  bool need_dq_acc, need_dkdv_acc, group_tmem, need_fold;
 };
 
 Derived derive(const gqa_attn_params* p, void* ws) {
@@ -93,6 +94,7 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   d.group_tmem = p->deterministic || p->group_mode == GQA_GROUP_TMEM;
   d.need_dq_acc = !p->deterministic && kv_kernel_has_dq(p->Dqk);
   d.need_dkdv_acc = !d.group_tmem;
+  d.need_fold = kv_kernel_folds_stats(p->Dqk);
   Problem& pr = d.pr;
   pr.B = p->B;
   pr.Hq = p->Hq;
@@ -110,11 +112,13 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   pr.max_len = p->cu_seqlens ? p->max_seqlen : p->S;
   pr.ntiles = (pr.max_len + kStatTile - 1) / kStatTile;
   pr.wait_limit = g_wait_limit.load();
-  d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc, d.need_dkdv_acc);
+  d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc, d.need_dkdv_acc,
+                   d.need_fold);
   uint8_t* base = static_cast<uint8_t*>(ws);
   pr.err = reinterpret_cast<int*>(base + d.ws.err_off);
   pr.nlse2 = reinterpret_cast<float*>(base + d.ws.lse2_off);
   pr.ndelta = reinterpret_cast<float*>(base + d.ws.delta_off);
+  pr.xfold = d.need_fold ? base + d.ws.xf_off : nullptr;
   pr.dq_acc = d.need_dq_acc ? reinterpret_cast<float*>(base + d.ws.dq_off) : nullptr;
   pr.dk_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dk_off) : nullptr;
   pr.dv_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dv_off) : nullptr;

@@ -34,6 +34,9 @@ struct Problem {
   float* nlse2;       // [Hq][nseqs][ntiles][128]  -LSE * log2(e), -inf on padding rows
   float* ndelta;      // same layout, -Delta, 0 on padding rows (both negated so the
                       // kernels use one packed fma / add per pair of elements)
+  uint8_t* xfold;     // or null: [Hq][nseqs][ntiles] 4 KB tiles, one 32-byte fp16 row per query:
+                      // -LSE/scale and -Delta, each split hi + lo, in the tensor core's
+                      // no-swizzle K-major layout (the main kernel adds them with an MMA)
   float* dq_acc;      // [B][Hq][S][Dqk] fp32
   float* dk_acc;      // [B][Hkv][S][Dqk] fp32
   float* dv_acc;      // [B][Hkv][S][Dv] fp32
@@ -77,13 +80,15 @@ __host__ __device__ __forceinline__ size_t stat_index(const Problem& p, int h, i
 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-  size_t err_off, lse2_off, delta_off, dq_off, dk_off, dv_off, total;
+  size_t err_off, lse2_off, delta_off, xf_off, dq_off, dk_off, dv_off, total;
 };
+
+constexpr int kFoldRowBytes = 32;  // 16 fp16 values per query row in an xfold tile
 
 __host__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 __host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Dqk, int Dv, int nseqs, int ntiles,
-                                   bool need_dq_acc, bool need_dkdv_acc) {
+                                   bool need_dq_acc, bool need_dkdv_acc, bool need_fold) {
   WsLayout w{};
   size_t off = 0;
   w.err_off = off;
@@ -93,6 +98,8 @@ __host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Dqk, int D
   off = align256(off + nstat * 4);
   w.delta_off = off;
   off = align256(off + nstat * 4);
+  w.xf_off = off;
+  if (need_fold) off = align256(off + nstat * kFoldRowBytes);
   w.dq_off = off;
   if (need_dq_acc) off = align256(off + static_cast<size_t>(B) * Hq * S * Dqk * 4);
   w.dk_off = off;

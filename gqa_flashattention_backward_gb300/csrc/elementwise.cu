@@ -40,6 +40,23 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int nseqs, int row) {
   return lo;
 }
 
+// One query row of an xfold tile: 16 fp16 values in the no-swizzle K-major core-matrix layout
+// (8 rows x 16 bytes per core matrix; the 8-row groups 256 bytes apart, the two K halves
+// 128 bytes apart).  K columns 0, 1 hold -LSE/scale as hi + lo; columns 8, 9 hold -Delta as
+// hi + lo; the rest are zero.  Adding this row through one K=16 MMA against a ones operand
+// subtracts LSE/scale from every logit of the row (resp. Delta from every dP) in fp32.
+__device__ __forceinline__ uint32_t split_hi_lo(float x) {
+  x = fminf(fmaxf(x, -60000.f), 60000.f);  // -inf (padding rows) -> a value that zeroes exp2
+  const __half hi = __float2half_rn(x);
+  const __half lo = __float2half_rn(x - __half2float(hi));
+  return static_cast<uint32_t>(__half_as_ushort(hi)) | (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
+}
+__device__ __forceinline__ void write_fold_row(uint8_t* tile, int q, float xl, float xd) {
+  uint8_t* row = tile + (q >> 3) * 256 + (q & 7) * 16;
+  *reinterpret_cast<uint4*>(row) = make_uint4(split_hi_lo(xl), 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(row + 128) = make_uint4(split_hi_lo(xd), 0u, 0u, 0u);
+}
+
 // 8 threads per row; each thread covers Dv/8 elements.
 template <typename T, int DV>
 __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __restrict__ o,
@@ -90,6 +107,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
         const size_t base = stat_index(p, h, s, il / kStatTile) + (il % kStatTile);
         p.nlse2[base] = -__ldg(lse + r) * kLog2e;
         p.ndelta[base] = -acc;
+        if (p.xfold)
+          write_fold_row(p.xfold + stat_index(p, h, s, il / kStatTile) * kFoldRowBytes, il % kStatTile,
+                         -__ldg(lse + r) / p.scale, -acc);
       } else if (il == 0) {
         atomicCAS(p.err, 0, kErrSeqTooLong);
       }
@@ -100,6 +120,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
       for (int pr = (len % kStatTile) + sub; pr < kStatTile; pr += 8) {
         p.nlse2[base + pr] = __int_as_float(0xff800000);  // -inf: exp2(x - inf) = 0
         p.ndelta[base + pr] = 0.f;
+        if (p.xfold) write_fold_row(p.xfold + base * kFoldRowBytes, pr, -INFINITY, 0.f);
       }
     }
     if (zero_dq) {

@@ -54,6 +54,11 @@ struct KvCfg {
   static constexpr int Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
   static constexpr int ST = 3;
   static constexpr int DS_BYTES = HAS_DQ ? BQ * BK * 2 : 0;   // one dS tile; two alternate
+  // head dim 64: -LSE/scale and -Delta enter Sᵀ and dPᵀ through one extra K=16 MMA each (an xfold
+  // tile per stage against constant ones operands) instead of per-element shared-memory loads
+  static constexpr bool FOLD = (DQK == 64);
+  static constexpr int X_BYTES = FOLD ? BQ * kFoldRowBytes : 0;
+  static constexpr int STAT_BYTES = FOLD ? 0 : BQ * 4;          // LSE / Delta vector per stage
   static constexpr int STG_BYTES = HAS_STAGING ? 4 * 32 * 32 * 4 : (DQ_T ? BQ * DQK * 4 : 0);
   // shared-memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_K = 0, OFF_V = OFF_K + K_BYTES;
@@ -61,9 +66,12 @@ struct KvCfg {
   static constexpr int OFF_DO = OFF_Q + ST * Q_BYTES;
   static constexpr int OFF_DS = OFF_DO + ST * DO_BYTES;
   static constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;
-  static constexpr int OFF_LSE = OFF_STG + STG_BYTES;           // ST x BQ floats
-  static constexpr int OFF_DEL = OFF_LSE + ST * BQ * 4;
-  static constexpr int OFF_CTL = OFF_DEL + ST * BQ * 4;
+  static constexpr int OFF_LSE = OFF_STG + STG_BYTES;           // ST x BQ floats (not FOLD)
+  static constexpr int OFF_DEL = OFF_LSE + ST * STAT_BYTES;
+  static constexpr int OFF_X = OFF_DEL + ST * STAT_BYTES;        // ST xfold tiles (FOLD)
+  static constexpr int OFF_ONES = OFF_X + ST * X_BYTES;          // FOLD: 3 core matrices ones|zeros|ones
+  static constexpr int ONES_BYTES = FOLD ? 384 : 0;
+  static constexpr int OFF_CTL = OFF_ONES + ONES_BYTES;
   static constexpr int SMEM = OFF_CTL + 256;
   // TMEM columns
   static constexpr uint32_t T_S = 0, T_DP = BQ, T_DV = 2 * BQ, T_DK = 2 * BQ + DV;
@@ -225,6 +233,13 @@ __global__ void __launch_bounds__(448, 1)
     tmem_alloc(&ctl.tmem_base, 512);
     tmem_relinquish();
   }
+  if (C::FOLD && tid < C::ONES_BYTES / 16) {
+    // fp16 core matrices ones | zeros | ones: the A operands that add the xfold columns 0-7
+    // (start 0) or 8-15 (start 128) of each query row to every logit of that row
+    const uint32_t v = (tid / 8 == 1) ? 0u : 0x3C003C00u;
+    reinterpret_cast<uint4*>(smem + C::OFF_ONES)[tid] = make_uint4(v, v, v, v);
+    fence_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -254,14 +269,17 @@ __global__ void __launch_bounds__(448, 1)
         const int qrow = sq.start + t * C::BQ;
         uint8_t* sQ = smem + C::OFF_Q + st * C::Q_BYTES;
         uint8_t* sDO = smem + C::OFF_DO + st * C::DO_BYTES;
-        float* sL = reinterpret_cast<float*>(smem + C::OFF_LSE) + st * C::BQ;
-        float* sD = reinterpret_cast<float*>(smem + C::OFF_DEL) + st * C::BQ;
         const size_t sidx = stat_index(p, h, s, (t * C::BQ) / kStatTile) + (t * C::BQ) % kStatTile;
-        mbar_expect_tx(&ctl.q_full[st], C::Q_BYTES + 2 * C::BQ * 4);
+        mbar_expect_tx(&ctl.q_full[st], C::Q_BYTES + (C::FOLD ? C::X_BYTES : 2 * C::STAT_BYTES));
         for (int cb = 0; cb < DQK / 64; ++cb)
           tma_load_3d(sQ + cb * (C::BQ * 128), &m.q, &ctl.q_full[st], cb * 64, qrow, zq);
-        bulk_load(sL, p.nlse2 + sidx, C::BQ * 4, &ctl.q_full[st]);
-        bulk_load(sD, p.ndelta + sidx, C::BQ * 4, &ctl.q_full[st]);
+        if (C::FOLD) {
+          // the tile's rows are contiguous in the xfold layout (whole 8-row groups)
+          bulk_load(smem + C::OFF_X + st * C::X_BYTES, p.xfold + sidx * kFoldRowBytes, C::X_BYTES, &ctl.q_full[st]);
+        } else {
+          bulk_load(smem + C::OFF_LSE + st * C::STAT_BYTES, p.nlse2 + sidx, C::STAT_BYTES, &ctl.q_full[st]);
+          bulk_load(smem + C::OFF_DEL + st * C::STAT_BYTES, p.ndelta + sidx, C::STAT_BYTES, &ctl.q_full[st]);
+        }
         mbar_expect_tx(&ctl.do_full[st], C::DO_BYTES);
         for (int cb = 0; cb < DV / 64; ++cb)
           tma_load_3d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.do_full[st], cb * 64, qrow, zq);
@@ -301,6 +319,11 @@ __global__ void __launch_bounds__(448, 1)
       const uint64_t dQ_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::BQ * 128, 1024);
       const uint64_t dDO_k0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
       const uint64_t dDO_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::BQ * 128, 1024);
+      // the fold: ones (A, fp16, no swizzle, one core matrix pair for every row group) x xfold tile (B)
+      constexpr uint32_t idF = idesc_f16(128, C::BQ, false, false, false);
+      const uint64_t dAL = sdesc_none(smem_u32(smem + C::OFF_ONES), 128, 0);        // K columns 0-7
+      const uint64_t dAD = sdesc_none(smem_u32(smem + C::OFF_ONES) + 128, 128, 0);  // K columns 8-15
+      const uint64_t dX0 = sdesc_none(smem_u32(smem + C::OFF_X), 128, 256);
       // K-major operand with 64-element (128-byte) rows: K step kk lives in 64-column block kk/4 at byte kk%4*32
       auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
       bool ok = mbar_wait_warp(&ctl.kv_full, 0, guard, 12);
@@ -312,6 +335,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk)
           umma_ss(tmem + C::T_S, desc_advance(dK_k, kstep(kk, C::BK)), desc_advance(dq, kstep(kk, C::BQ)), idS, kk > 0);
+        if (C::FOLD) umma_ss(tmem + C::T_S, dAL, desc_advance(dX0, st * C::X_BYTES), idF, 1u);  // - LSE/scale
         umma_commit(&ctl.s_full);
         return true;
       };
@@ -325,6 +349,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
           umma_ss(tmem + C::T_DP, desc_advance(dV_k, kstep(kk, C::BK)), desc_advance(ddo, kstep(kk, C::BQ)), idS, kk > 0);
+        if (C::FOLD) umma_ss(tmem + C::T_DP, dAD, desc_advance(dX0, st * C::X_BYTES), idF, 1u);  // - Delta
         umma_commit(&ctl.dp_full);
         return true;
       };
@@ -489,6 +514,20 @@ __global__ void __launch_bounds__(448, 1)
                              (p.window > 0 && i0 + C::BQ - 1 - j0 >= p.window);
       const float4* sL4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE) + (st * C::BQ + cbase) / 4;
       const float4* sD4 = reinterpret_cast<const float4*>(smem + C::OFF_DEL) + (st * C::BQ + cbase) / 4;
+      // exponent arguments of four consecutive columns: S*scale*log2e - LSE2 (with the fold the MMA
+      // already subtracted LSE/scale, so only the scaling remains)
+      auto exp_args = [&](const uint32_t* v4, const float4* l4, float2 s2, float2& x0, float2& x1) {
+        const float2 a = make_float2(__uint_as_float(v4[0]), __uint_as_float(v4[1]));
+        const float2 b = make_float2(__uint_as_float(v4[2]), __uint_as_float(v4[3]));
+        if constexpr (C::FOLD) {
+          x0 = mul2(a, s2);
+          x1 = mul2(b, s2);
+        } else {
+          const float4 l = *l4;
+          x0 = fma2(a, s2, make_float2(l.x, l.y));
+          x1 = fma2(b, s2, make_float2(l.z, l.w));
+        }
+      };
       if (!mbar_wait_warp(&ctl.q_full[st], (it / C::ST) & 1, guard, 20) ||
           !mbar_wait_warp(&ctl.s_full, it & 1, guard, 21)) {
         ok = false;
@@ -506,11 +545,8 @@ __global__ void __launch_bounds__(448, 1)
           float pf[32];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 l = sL4[8 * c + q4];
-            const float2 x0 = fma2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])), sl2,
-                                   make_float2(l.x, l.y));
-            const float2 x1 = fma2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])), sl2,
-                                   make_float2(l.z, l.w));
+            float2 x0, x1;
+            exp_args(v + 4 * q4, sL4 + 8 * c + q4, sl2, x0, x1);
             pf[4 * q4 + 0] = ex2_approx(x0.x);
             pf[4 * q4 + 1] = ex2_approx(x0.y);
             pf[4 * q4 + 2] = ex2_approx(x1.x);
@@ -523,11 +559,8 @@ __global__ void __launch_bounds__(448, 1)
           // result is the packed P the MMA consumes (argument rounding adds at most ~2e-4 to P)
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 l = sL4[8 * c + q4];
-            const float2 x0 = fma2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])), sl2,
-                                   make_float2(l.x, l.y));
-            const float2 x1 = fma2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])), sl2,
-                                   make_float2(l.z, l.w));
+            float2 x0, x1;
+            exp_args(v + 4 * q4, sL4 + 8 * c + q4, sl2, x0, x1);
             pk[16 * c + 2 * q4] = ex2_f16x2(pack2<false>(x0.x, x0.y));
             pk[16 * c + 2 * q4 + 1] = ex2_f16x2(pack2<false>(x1.x, x1.y));
           }
@@ -568,11 +601,13 @@ __global__ void __launch_bounds__(448, 1)
         uint32_t ds[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 d = sD4[8 * c + q4];
-          const float2 a = add2(make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1])),
-                                make_float2(d.x, d.y));
-          const float2 b = add2(make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])),
-                                make_float2(d.z, d.w));
+          float2 a = make_float2(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]));
+          float2 b = make_float2(__uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+          if constexpr (!C::FOLD) {  // with the fold the MMA already subtracted Delta
+            const float4 d = sD4[8 * c + q4];
+            a = add2(a, make_float2(d.x, d.y));
+            b = add2(b, make_float2(d.z, d.w));
+          }
           ds[2 * q4] = mul_packed<BF16>(pk[16 * c + 2 * q4], pack2<BF16>(a.x, a.y));
           ds[2 * q4 + 1] = mul_packed<BF16>(pk[16 * c + 2 * q4 + 1], pack2<BF16>(b.x, b.y));
         }
@@ -677,6 +712,7 @@ cudaError_t launch_bwd_kv(const Problem& p, int dtype_bf16, const Maps& m, const
 }
 
 bool kv_kernel_has_dq(int Dqk) { return Dqk != 192; }
+bool kv_kernel_folds_stats(int Dqk) { return Dqk == 64; }
 bool kv_kernel_has_bulk_dq(int Dqk) { return Dqk != 192; }
 int kv_kernel_bq(int Dqk) { return Dqk == 64 ? 128 : 64; }
 

@@ -176,6 +176,17 @@ __device__ __forceinline__ void tc_fence_after() {
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B: 128-byte rows, 8-row / 1024-byte atoms, 16-byte
 // chunk index XOR row-in-atom). lbo/sbo in bytes.
+// Shared-memory matrix descriptor without swizzle: 8-row x 16-byte core matrices; for a K-major
+// operand `lbo` is the byte distance between core matrices adjacent along K and `sbo` between
+// core matrices adjacent along M / N (0 repeats one core matrix for every row group).
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version for the tcgen05 path; swizzle mode 0
+  return d;
+}
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
