@@ -11,8 +11,11 @@ the C ABI prescribes:
 * :func:`gqa_attention` -> both, as a ``torch.autograd.Function`` (O from the
   forward, dQ / dK / dV / dsink from the backward when autograd asks for them).
 
-Tensors use the BHSD layout: q [B,Hq,S,Dqk], k [B,Hkv,S,Dqk], v [B,Hkv,S,Dv],
-o/dout [B,Hq,S,Dv]; packed variable-length batches use B=1 and ``cu_seqlens``.
+Tensors have shape q [B,Hq,S,Dqk], k [B,Hkv,S,Dqk], v [B,Hkv,S,Dv], o/dout [B,Hq,S,Dv]
+and any layout whose head dim is contiguous (BHSD, a BSHD view ``x.transpose(1, 2)``, packed
+THD for varlen as ``x.permute(1, 0, 2).unsqueeze(0)``): the strides go to the kernels, nothing
+is copied; outputs take the layout of the matching input.  Packed variable-length batches use
+B=1 and ``cu_seqlens``.
 """
 from __future__ import annotations
 
@@ -37,17 +40,29 @@ def preferred_red_mode(Dqk: int) -> int:
 
 
 def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=GQA_GROUP_TMEM,
-            red_mode=None, deterministic=False):
+            red_mode=None, deterministic=False, **tensors):
+    """`tensors`: any of o, do, dq, dk, dv whose layouts the call uses."""
     B, Hq, S, Dqk = q.shape
     if red_mode is None:
         red_mode = preferred_red_mode(Dqk)
     Hkv, Dv = k.shape[1], v.shape[3]
     for t in (q, k, v):
-        if not (t.is_cuda and t.is_contiguous() and t.dtype == q.dtype):
-            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype")
+        if not (t.is_cuda and t.dtype == q.dtype):
+            raise ValueError("q, k, v must be CUDA tensors of one dtype")
+    named = dict(q=q, k=k, v=v, **{n: t for n, t in tensors.items() if t is not None})
+    strides = {n: native.tensor_strides(t) for n, t in named.items()}
     return native.make_params(B, Hq, Hkv, S, Dqk, Dv, q.dtype, causal=causal, window=window, scale=scale,
                               cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, group_mode=group_mode,
-                              red_mode=red_mode, deterministic=deterministic)
+                              red_mode=red_mode, deterministic=deterministic, strides=strides)
+
+
+def _empty_like_layout(ref: torch.Tensor, last_dim: int) -> torch.Tensor:
+    """An uninitialised [B, H, S, last_dim] tensor whose dims are ordered in memory like ref's."""
+    order = sorted(range(3), key=lambda i: -ref.stride(i))  # outermost first
+    shape = [ref.shape[i] for i in order] + [last_dim]
+    t = torch.empty(shape, dtype=ref.dtype, device=ref.device)
+    inv = [order.index(i) for i in range(3)] + [3]
+    return t.permute(*inv)
 
 
 def attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = True, window: int = 0,
@@ -55,9 +70,9 @@ def attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, caus
                       cu_seqlens: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
                       workspace: Optional[torch.Tensor] = None):
     """Returns (o, lse): o [B,Hq,S,Dv] in q's dtype, lse [B,Hq,S] fp32 (natural log, sink included)."""
-    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen)
     B, Hq, S, _ = q.shape
-    o = torch.empty((B, Hq, S, v.shape[3]), dtype=q.dtype, device=q.device)
+    o = _empty_like_layout(q, v.shape[3])
+    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, o=o)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     ws = workspace if workspace is not None else native.alloc_workspace(p, q.device)
     native.fwd(p, q, k, v, sink, o, lse, ws)
@@ -72,17 +87,18 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                        workspace: Optional[torch.Tensor] = None, out: Optional[dict] = None) -> dict:
     """Returns dict(dq, dk, dv, delta[, dsink]).  `out` may hold preallocated tensors of the same names.
     red_mode None picks :func:`preferred_red_mode`."""
-    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode, red_mode, deterministic)
     B, Hq, S, Dqk = q.shape
     Hkv, Dv = k.shape[1], v.shape[3]
     res = dict(out) if out else {}
     dev = q.device
     if "dq" not in res:
-        res["dq"] = torch.empty_like(q)
+        res["dq"] = _empty_like_layout(q, Dqk)
     if "dk" not in res:
-        res["dk"] = torch.empty_like(k)
+        res["dk"] = _empty_like_layout(k, Dqk)
     if "dv" not in res:
-        res["dv"] = torch.empty_like(v)
+        res["dv"] = _empty_like_layout(v, Dv)
+    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode, red_mode, deterministic,
+                o=o, do=dout, dq=res["dq"], dk=res["dk"], dv=res["dv"])
     if "delta" not in res:
         res["delta"] = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
     if sink is not None and "dsink" not in res:

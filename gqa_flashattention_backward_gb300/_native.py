@@ -31,7 +31,7 @@ GQA_RED_V4, GQA_RED_BULK, GQA_RED_SCALAR, GQA_RED_NONE = 0, 1, 2, 3
 EXPORTS = (
     "gqa_attn_workspace_size", "gqa_attn_fwd", "gqa_attn_bwd_preprocess", "gqa_attn_bwd",
     "gqa_attn_bwd_postprocess", "gqa_attn_dsink", "gqa_attn_get_device_error", "gqa_attn_set_wait_limit",
-    "gqa_attn_selftest_wait_timeout", "gqa_attn_strerror", "gqa_attn_bwd_noalloc",
+    "gqa_attn_selftest_wait_timeout", "gqa_attn_strerror", "gqa_attn_bwd_noalloc", "gqa_attn_params_size",
 )
 
 
@@ -41,6 +41,14 @@ class GqaError(RuntimeError):
         super().__init__(f"{what}: {strerror(status)} ({status})")
 
 
+class Stride(ctypes.Structure):
+    """gqa_stride: element strides along batch, head, sequence ({0,0,0} = contiguous BHSD)."""
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("s", ctypes.c_int64)]
+
+
+STRIDE_FIELDS = ("q_st", "k_st", "v_st", "o_st", "do_st", "dq_st", "dk_st", "dv_st")
+
+
 class Params(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("S", ctypes.c_int),
@@ -48,7 +56,7 @@ class Params(ctypes.Structure):
         ("window", ctypes.c_int), ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p),
         ("nseq", ctypes.c_int), ("max_seqlen", ctypes.c_int), ("group_mode", ctypes.c_int),
         ("red_mode", ctypes.c_int), ("deterministic", ctypes.c_int),
-    ]
+    ] + [(n, Stride) for n in STRIDE_FIELDS]
 
 
 _lib = None
@@ -70,6 +78,11 @@ def load():
     vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     lib.gqa_attn_workspace_size.argtypes = [P]
     lib.gqa_attn_workspace_size.restype = sz
+    lib.gqa_attn_params_size.argtypes = []
+    lib.gqa_attn_params_size.restype = sz
+    if lib.gqa_attn_params_size() != ctypes.sizeof(Params):
+        raise ImportError(f"gqa_attn_params is {lib.gqa_attn_params_size()} bytes in {_LIB_PATH}, "
+                          f"{ctypes.sizeof(Params)} in this binding: rebuild the library")
     lib.gqa_attn_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.gqa_attn_fwd.restype = st
     lib.gqa_attn_bwd_preprocess.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
@@ -114,9 +127,11 @@ def _check(status: int, what: str):
 
 
 def make_params(B, Hq, Hkv, S, Dqk, Dv, dtype, causal=True, window=0, scale=None, cu_seqlens=None,
-                max_seqlen=None, group_mode=GQA_GROUP_TMEM, red_mode=GQA_RED_V4, deterministic=False) -> Params:
+                max_seqlen=None, group_mode=GQA_GROUP_TMEM, red_mode=GQA_RED_V4, deterministic=False,
+                strides=None) -> Params:
     """Build the parameter struct.  `dtype` is a torch dtype (float16/bfloat16);
-    `cu_seqlens` a device int32 tensor or None."""
+    `cu_seqlens` a device int32 tensor or None; `strides` maps some of "q", "k", "v", "o", "do",
+    "dq", "dk", "dv" to (batch, head, sequence) element strides (missing: contiguous BHSD)."""
     p = Params()
     p.B, p.Hq, p.Hkv, p.S, p.Dqk, p.Dv = int(B), int(Hq), int(Hkv), int(S), int(Dqk), int(Dv)
     p.dtype = GQA_BF16 if dtype == torch.bfloat16 else (GQA_F16 if dtype == torch.float16 else -1)
@@ -134,7 +149,20 @@ def make_params(B, Hq, Hkv, S, Dqk, Dv, dtype, causal=True, window=0, scale=None
     p.group_mode = int(group_mode)
     p.red_mode = int(red_mode)
     p.deterministic = int(bool(deterministic))
+    for name, st in (strides or {}).items():
+        s = getattr(p, name + "_st")
+        s.b, s.h, s.s = (int(x) for x in st)
     return p
+
+
+def tensor_strides(t: torch.Tensor):
+    """(batch, head, sequence) element strides of a [B, H, S, D] tensor whose last dim is contiguous."""
+    if t.dim() != 4 or (t.stride(3) != 1 and t.shape[3] > 1):
+        raise ValueError("tensors must be [B, H, S, D] with a contiguous head dim")
+    _, H, S, D = t.shape
+    default = (H * S * D, S * D, D)
+    # a dim of size 1 (or an empty tensor) may carry any stride: the kernels never step along it
+    return tuple(default[i] if t.shape[i] <= 1 or t.numel() == 0 else t.stride(i) for i in range(3))
 
 
 def workspace_size(p: Params) -> int:

@@ -56,6 +56,23 @@ bool supported_dims(int dqk, int dv) {
   return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
 }
 
+bool is_default(const gqa_stride& s) { return s.b == 0 && s.h == 0 && s.s == 0; }
+
+// An explicit layout: 16-byte multiples, rows at least D elements apart, batch stride 0 only for B == 1.
+bool valid_stride(const gqa_stride& s, int B, int D) {
+  if (is_default(s)) return true;
+  if (s.h % 8 || s.s % 8 || s.b % 8) return false;
+  if (s.h < D || s.s < D || s.b < 0) return false;
+  if (s.b == 0 && B > 1) return false;
+  return true;
+}
+
+Strides resolve(const gqa_stride& s, int B, int H, int S, int D) {
+  if (is_default(s)) return Strides{static_cast<long long>(H) * S * D, static_cast<long long>(S) * D, D};
+  // with one batch the batch stride is never used; any valid value keeps the tensor map legal
+  return Strides{s.b != 0 ? s.b : static_cast<long long>(H) * S * D, s.h, s.s};
+}
+
 gqa_status validate(const gqa_attn_params* p) {
   if (!p) return GQA_ERR_INVALID_ARG;
   if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->S < 0) return GQA_ERR_INVALID_ARG;
@@ -64,6 +81,11 @@ gqa_status validate(const gqa_attn_params* p) {
   if (p->causal != 0 && p->causal != 1) return GQA_ERR_INVALID_ARG;
   if (p->window > 0 && !p->causal) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(p->scale) || !(p->scale > 0.f)) return GQA_ERR_INVALID_ARG;
+  if (p->S > 0 && (!valid_stride(p->q_st, p->B, p->Dqk) || !valid_stride(p->k_st, p->B, p->Dqk) ||
+      !valid_stride(p->v_st, p->B, p->Dv) || !valid_stride(p->o_st, p->B, p->Dv) ||
+      !valid_stride(p->do_st, p->B, p->Dv) || !valid_stride(p->dq_st, p->B, p->Dqk) ||
+      !valid_stride(p->dk_st, p->B, p->Dqk) || !valid_stride(p->dv_st, p->B, p->Dv)))
+    return GQA_ERR_INVALID_ARG;
   if (p->group_mode != GQA_GROUP_TMEM && p->group_mode != GQA_GROUP_ATOMIC) return GQA_ERR_INVALID_ARG;
   if (p->red_mode < GQA_RED_V4 || p->red_mode > GQA_RED_NONE) return GQA_ERR_INVALID_ARG;
   if (p->deterministic != 0 && p->deterministic != 1) return GQA_ERR_INVALID_ARG;
@@ -112,6 +134,14 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   pr.max_len = p->cu_seqlens ? p->max_seqlen : p->S;
   pr.ntiles = (pr.max_len + kStatTile - 1) / kStatTile;
   pr.wait_limit = g_wait_limit.load();
+  pr.q_st = resolve(p->q_st, p->B, p->Hq, p->S, p->Dqk);
+  pr.k_st = resolve(p->k_st, p->B, p->Hkv, p->S, p->Dqk);
+  pr.v_st = resolve(p->v_st, p->B, p->Hkv, p->S, p->Dv);
+  pr.o_st = resolve(p->o_st, p->B, p->Hq, p->S, p->Dv);
+  pr.do_st = resolve(p->do_st, p->B, p->Hq, p->S, p->Dv);
+  pr.dq_st = resolve(p->dq_st, p->B, p->Hq, p->S, p->Dqk);
+  pr.dk_st = resolve(p->dk_st, p->B, p->Hkv, p->S, p->Dqk);
+  pr.dv_st = resolve(p->dv_st, p->B, p->Hkv, p->S, p->Dv);
   d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc, d.need_dkdv_acc,
                    d.need_fold);
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -131,14 +161,19 @@ gqa_status check_ws(const gqa_attn_params* p, void* ws, size_t bytes) {
   return GQA_OK;
 }
 
-bool map16(CUtensorMap* m, const void* ptr, int D, int S, int Z, int box_rows, bool bf16) {
+// A 16-bit [B, H, S, D] tensor with element strides st as a 4-D TMA tensor (D, S, H, B); the box is
+// 64 columns x box_rows rows of one (b, h), 128-byte swizzled.  Tiles past a head's last row read
+// zeros and never cross into another head, whatever the layout.
+bool map16(CUtensorMap* m, const void* ptr, int D, int S, int H, int B, const Strides& st, int box_rows, bool bf16) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(Z)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr),
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.s) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                           static_cast<cuuint64_t>(st.b) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr),
              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -161,6 +196,8 @@ gqa_status to_status(cudaError_t e) { return e == cudaSuccess ? GQA_OK : GQA_ERR
 
 extern "C" {
 
+size_t gqa_attn_params_size(void) { return sizeof(gqa_attn_params); }
+
 size_t gqa_attn_workspace_size(const gqa_attn_params* p) {
   if (validate(p) != GQA_OK) return 0;
   return derive(p, nullptr).ws.total;
@@ -181,8 +218,8 @@ gqa_status gqa_attn_fwd(const gqa_attn_params* p, const void* q, const void* k, 
   Maps m;
   std::memset(&m, 0, sizeof(m));
   const int bk = q_kernel_bk();
-  if (!map16(&m.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) || !map16(&m.k, k, p->Dqk, p->S, p->B * p->Hkv, bk, bf) ||
-      !map16(&m.v, v, p->Dv, p->S, p->B * p->Hkv, bk, bf))
+  if (!map16(&m.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, 128, bf) || !map16(&m.k, k, p->Dqk, p->S, p->Hkv, p->B, d.pr.k_st, bk, bf) ||
+      !map16(&m.v, v, p->Dv, p->S, p->Hkv, p->B, d.pr.v_st, bk, bf))
     return GQA_ERR_CUDA;
   return to_status(launch_fwd(d.pr, bf, m, sink, o, lse, static_cast<cudaStream_t>(stream)));
 }
@@ -216,8 +253,8 @@ gqa_status gqa_attn_bwd(const gqa_attn_params* p, const void* q, const void* k, 
   const int bq = kv_kernel_bq(p->Dqk);
   Maps m;
   std::memset(&m, 0, sizeof(m));
-  if (!map16(&m.q, q, p->Dqk, p->S, p->B * p->Hq, bq, bf) || !map16(&m.dout, dout, p->Dv, p->S, p->B * p->Hq, bq, bf) ||
-      !map16(&m.k, k, p->Dqk, p->S, p->B * p->Hkv, 128, bf) || !map16(&m.v, v, p->Dv, p->S, p->B * p->Hkv, 128, bf))
+  if (!map16(&m.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, bq, bf) || !map16(&m.dout, dout, p->Dv, p->S, p->Hq, p->B, d.pr.do_st, bq, bf) ||
+      !map16(&m.k, k, p->Dqk, p->S, p->Hkv, p->B, d.pr.k_st, 128, bf) || !map16(&m.v, v, p->Dv, p->S, p->Hkv, p->B, d.pr.v_st, 128, bf))
     return GQA_ERR_CUDA;
   if (d.need_dq_acc && !map32(&m.dq_acc, d.pr.dq_acc, p->Dqk, p->S, p->B * p->Hq)) return GQA_ERR_CUDA;
   if (d.need_dkdv_acc && (!map32(&m.dk_acc, d.pr.dk_acc, p->Dqk, p->S, p->B * p->Hkv) ||
@@ -236,9 +273,9 @@ gqa_status gqa_attn_bwd(const gqa_attn_params* p, const void* q, const void* k, 
   if (dq_pass) {
     Maps m2 = m;  // the query-stationary pass: 128-row Q / dO boxes, K / V boxes of its key tile
     const int bk = q_kernel_bk();
-    if (!map16(&m2.q, q, p->Dqk, p->S, p->B * p->Hq, 128, bf) ||
-        !map16(&m2.dout, dout, p->Dv, p->S, p->B * p->Hq, 128, bf) ||
-        !map16(&m2.k, k, p->Dqk, p->S, p->B * p->Hkv, bk, bf) || !map16(&m2.v, v, p->Dv, p->S, p->B * p->Hkv, bk, bf))
+    if (!map16(&m2.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, 128, bf) ||
+        !map16(&m2.dout, dout, p->Dv, p->S, p->Hq, p->B, d.pr.do_st, 128, bf) ||
+        !map16(&m2.k, k, p->Dqk, p->S, p->Hkv, p->B, d.pr.k_st, bk, bf) || !map16(&m2.v, v, p->Dv, p->S, p->Hkv, p->B, d.pr.v_st, bk, bf))
       return GQA_ERR_CUDA;
     e = launch_dq(d.pr, bf, m2, dq, st);
     if (e != cudaSuccess) return GQA_ERR_CUDA;
@@ -259,14 +296,12 @@ gqa_status gqa_attn_bwd_postprocess(const gqa_attn_params* p, void* dq, void* dk
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int sms = num_sms();
   if (d.need_dq_acc) {
-    cudaError_t e = launch_cast(d.pr.dq_acc, dq, static_cast<long long>(p->B) * p->Hq * p->S * p->Dqk, p->scale, bf,
-                                sms, st);
+    cudaError_t e = launch_cast(d.pr.dq_acc, dq, p->B, p->Hq, p->S, p->Dqk, d.pr.dq_st, p->scale, bf, sms, st);
     if (e != cudaSuccess) return GQA_ERR_CUDA;
   }
   if (d.need_dkdv_acc) {
-    const long long rows = static_cast<long long>(p->B) * p->Hkv * p->S;
-    cudaError_t e = launch_cast(d.pr.dk_acc, dk, rows * p->Dqk, p->scale, bf, sms, st);
-    if (e == cudaSuccess) e = launch_cast(d.pr.dv_acc, dv, rows * p->Dv, 1.f, bf, sms, st);
+    cudaError_t e = launch_cast(d.pr.dk_acc, dk, p->B, p->Hkv, p->S, p->Dqk, d.pr.dk_st, p->scale, bf, sms, st);
+    if (e == cudaSuccess) e = launch_cast(d.pr.dv_acc, dv, p->B, p->Hkv, p->S, p->Dv, d.pr.dv_st, 1.f, bf, sms, st);
     if (e != cudaSuccess) return GQA_ERR_CUDA;
   }
   return GQA_OK;

@@ -18,6 +18,14 @@ enum : int {
   kErrBadSeqlens = 0x40000002,
 };
 
+// Element strides of a 16-bit [B, H, S, D] tensor (head-dim stride 1), resolved on the host.
+struct Strides {
+  long long b, h, s;
+  __host__ __device__ __forceinline__ long long row(int bi, int hi, long long si) const {
+    return bi * b + hi * h + si * s;
+  }
+};
+
 // Everything a kernel needs to know about the attention problem.
 struct Problem {
   int B, Hq, Hkv, S, Dqk, Dv, G;  // G = Hq / Hkv
@@ -40,6 +48,8 @@ struct Problem {
   float* dq_acc;      // [B][Hq][S][Dqk] fp32
   float* dk_acc;      // [B][Hkv][S][Dqk] fp32
   float* dv_acc;      // [B][Hkv][S][Dv] fp32
+  // layouts of the caller's 16-bit tensors (element offset of row (b, h, s) = row(b, h, s))
+  Strides q_st, k_st, v_st, o_st, do_st, dq_st, dk_st, dv_st;
 };
 
 // One sequence of the (possibly packed) batch.

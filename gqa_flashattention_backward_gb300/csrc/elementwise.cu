@@ -69,8 +69,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
   const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 3);
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 3) + (threadIdx.x >> 3); r < nrows;
        r += stride) {
-    const uint4* po = reinterpret_cast<const uint4*>(o + r * DV + sub * PER);
-    const uint4* pd = reinterpret_cast<const uint4*>(dout + r * DV + sub * PER);
+    const int i = static_cast<int>(r % p.S);
+    const int h = static_cast<int>((r / p.S) % p.Hq);
+    const int b = static_cast<int>(r / (static_cast<long long>(p.S) * p.Hq));
+    const uint4* po = reinterpret_cast<const uint4*>(o + p.o_st.row(b, h, i) + sub * PER);
+    const uint4* pd = reinterpret_cast<const uint4*>(dout + p.do_st.row(b, h, i) + sub * PER);
     float acc = 0.f;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
@@ -86,9 +89,6 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    const int i = static_cast<int>(r % p.S);
-    const int h = static_cast<int>((r / p.S) % p.Hq);
-    const int b = static_cast<int>(r / (static_cast<long long>(p.S) * p.Hq));
     int s, il, len;
     if (p.cu_seqlens) {
       s = find_seq(p.cu_seqlens, p.nseqs, i);
@@ -137,22 +137,28 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
   }
 }
 
-// out[e] = dtype(acc[e] * mul), 8 elements per thread-iteration.
+// out row (b, h, s) = dtype(acc row * mul): acc is contiguous fp32 [B, H, S, D], out has the caller's
+// layout; 8 elements (one 16-byte store) per thread-iteration.
 template <typename T>
-__global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ acc, T* __restrict__ out, long long n,
-                                                   float mul) {
-  const long long n8 = n / 8;
+__global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ acc, T* __restrict__ out, int H, int S,
+                                                   int D, Strides st, long long n8, float mul) {
+  const int per_row = D / 8;
   for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
        e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = e / per_row;
+    const int c8 = static_cast<int>(e - row * per_row);
+    const int s = static_cast<int>(row % S);
+    const int h = static_cast<int>((row / S) % H);
+    const int b = static_cast<int>(row / (static_cast<long long>(S) * H));
     const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * e);
-    const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * e + 1);
+    const float4 c = __ldg(reinterpret_cast<const float4*>(acc) + 2 * e + 1);
     uint4 r;
     constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
     r.x = pack2<BF>(a.x * mul, a.y * mul);
     r.y = pack2<BF>(a.z * mul, a.w * mul);
-    r.z = pack2<BF>(b.x * mul, b.y * mul);
-    r.w = pack2<BF>(b.z * mul, b.w * mul);
-    reinterpret_cast<uint4*>(out)[e] = r;
+    r.z = pack2<BF>(c.x * mul, c.y * mul);
+    r.w = pack2<BF>(c.z * mul, c.w * mul);
+    *reinterpret_cast<uint4*>(out + st.row(b, h, s) + 8 * c8) = r;
   }
 }
 
@@ -217,18 +223,20 @@ cudaError_t launch_preprocess(const Problem& p, int dtype_bf16, const void* o, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_cast(const float* acc, void* out, long long n, float mul, int dtype_bf16, int num_sms,
-                        cudaStream_t st) {
-  if (n <= 0) return cudaSuccess;
-  long long blocks = (n / 8 + 255) / 256;
+cudaError_t launch_cast(const float* acc, void* out, int B, int H, int S, int D, const Strides& st, float mul,
+                        int dtype_bf16, int num_sms, cudaStream_t st_) {
+  const long long n8 = static_cast<long long>(B) * H * S * (D / 8);
+  if (n8 <= 0) return cudaSuccess;
+  long long blocks = (n8 + 255) / 256;
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (dtype_bf16)
-    cast_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        acc, static_cast<__nv_bfloat16*>(out), n, mul);
+    cast_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st_>>>(
+        acc, static_cast<__nv_bfloat16*>(out), H, S, D, st, n8, mul);
   else
-    cast_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, st>>>(acc, static_cast<__half*>(out), n, mul);
+    cast_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, st_>>>(acc, static_cast<__half*>(out), H, S, D, st,
+                                                                         n8, mul);
   return cudaGetLastError();
 }
 

@@ -256,23 +256,22 @@ __global__ void __launch_bounds__(448, 1)
       mbar_expect_tx(&ctl.kv_full, C::K_BYTES + C::V_BYTES);
       const int krow = sq.start + j0;
       for (int cb = 0; cb < DQK / 64; ++cb)
-        tma_load_3d(smem + C::OFF_K + cb * (C::BK * 128), &m.k, &ctl.kv_full, cb * 64, krow, zk);
+        tma_load_4d(smem + C::OFF_K + cb * (C::BK * 128), &m.k, &ctl.kv_full, cb * 64, krow, g, sq.b);
       for (int cb = 0; cb < DV / 64; ++cb)
-        tma_load_3d(smem + C::OFF_V + cb * (C::BK * 128), &m.v, &ctl.kv_full, cb * 64, krow, zk);
+        tma_load_4d(smem + C::OFF_V + cb * (C::BK * 128), &m.v, &ctl.kv_full, cb * 64, krow, g, sq.b);
       int issued = 0;
       for (int it = 0; it < NIT; ++it) {
         const int st = it % C::ST;
         if (it >= C::ST && !mbar_wait(&ctl.q_empty[st], ((it / C::ST) - 1) & 1, guard, 11)) break;
         const int h = h_first + it / nt;
         const int t = t0 + it % nt;
-        const int zq = sq.b * p.Hq + h;
         const int qrow = sq.start + t * C::BQ;
         uint8_t* sQ = smem + C::OFF_Q + st * C::Q_BYTES;
         uint8_t* sDO = smem + C::OFF_DO + st * C::DO_BYTES;
         const size_t sidx = stat_index(p, h, s, (t * C::BQ) / kStatTile) + (t * C::BQ) % kStatTile;
         mbar_expect_tx(&ctl.q_full[st], C::Q_BYTES + (C::FOLD ? C::X_BYTES : 2 * C::STAT_BYTES));
         for (int cb = 0; cb < DQK / 64; ++cb)
-          tma_load_3d(sQ + cb * (C::BQ * 128), &m.q, &ctl.q_full[st], cb * 64, qrow, zq);
+          tma_load_4d(sQ + cb * (C::BQ * 128), &m.q, &ctl.q_full[st], cb * 64, qrow, h, sq.b);
         if (C::FOLD) {
           // the tile's rows are contiguous in the xfold layout (whole 8-row groups)
           bulk_load(smem + C::OFF_X + st * C::X_BYTES, p.xfold + sidx * kFoldRowBytes, C::X_BYTES, &ctl.q_full[st]);
@@ -282,7 +281,7 @@ __global__ void __launch_bounds__(448, 1)
         }
         mbar_expect_tx(&ctl.do_full[st], C::DO_BYTES);
         for (int cb = 0; cb < DV / 64; ++cb)
-          tma_load_3d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.do_full[st], cb * 64, qrow, zq);
+          tma_load_4d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.do_full[st], cb * 64, qrow, h, sq.b);
         issued = it + 1;
       }
       if (ctl.abort_flag) {
@@ -636,7 +635,8 @@ __global__ void __launch_bounds__(448, 1)
       const size_t krow = static_cast<size_t>(zk) * p.S + sq.start + j;
       uint8_t* stg = smem + C::OFF_Q + warp * (2 * 32 * 32 * 4);  // stage buffers are idle now
       int nbulk = 0;
-      auto emit = [&](uint32_t tcol, int D, void* out, float* acc, const CUtensorMap* map, float mul) {
+      auto emit = [&](uint32_t tcol, int D, void* out, const Strides& ost, float* acc, const CUtensorMap* map,
+                      float mul) {
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t v[32];
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(448, 1)
             for (int e = 0; e < 32; ++e) v[e] = 0u;
           if (group_tmem) {
             if (valid) {
-              T* o = static_cast<T*>(out) + krow * D + c0;
+              T* o = static_cast<T*>(out) + ost.row(sq.b, g, sq.start + j) + c0;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 uint4 w;
@@ -671,8 +671,8 @@ __global__ void __launch_bounds__(448, 1)
           }
         }
       };
-      if (wg == 0) emit(C::T_DV, DV, dv_out, p.dv_acc, &m.dv_acc, 1.f);
-      else emit(C::T_DK, DQK, dk_out, p.dk_acc, &m.dk_acc, p.scale);
+      if (wg == 0) emit(C::T_DV, DV, dv_out, p.dv_st, p.dv_acc, &m.dv_acc, 1.f);
+      else emit(C::T_DK, DQK, dk_out, p.dk_st, p.dk_acc, &m.dk_acc, p.scale);
       if (lane == 0 && nbulk > 0) bulk_wait0();
       __syncwarp();
     }

@@ -8,7 +8,8 @@ namespace gqa {
 
 // Tensor maps of one call (built on the host, passed by value to kernels).
 struct Maps {
-  CUtensorMap q, k, v, o, dout;  // 16-bit tensors, 128B swizzle, box 64 x rows
+  CUtensorMap q, k, v, o, dout;  // 16-bit tensors as 4-D (D, S, H, B) with the caller's strides,
+                                 // 128B swizzle, box 64 columns x rows of one (b, h)
   CUtensorMap dq_acc;            // fp32 [B*Hq][S][Dqk], box 32 x 32, 128B swizzle (bulk reduce)
   CUtensorMap dk_acc, dv_acc;    // fp32 [B*Hkv][S][D]
 };
@@ -25,8 +26,8 @@ struct KvLaunch {
 
 cudaError_t launch_preprocess(const Problem& p, int dtype_bf16, const void* o, const void* dout, const float* lse,
                               float* delta, bool zero_dq, bool zero_dkdv, int num_sms, cudaStream_t st);
-cudaError_t launch_cast(const float* acc, void* out, long long n, float mul, int dtype_bf16, int num_sms,
-                        cudaStream_t st);
+cudaError_t launch_cast(const float* acc, void* out, int B, int H, int S, int D, const Strides& st, float mul,
+                        int dtype_bf16, int num_sms, cudaStream_t st_);
 cudaError_t launch_dsink(int B, int Hq, int S, const float* sink, const float* lse, const float* delta,
                          float* dsink, cudaStream_t st);
 cudaError_t launch_selftest_wait(int* err, long long limit, cudaStream_t st);

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(320, 1)
   const int n = k1 - k0;
   const int NIT = FWD ? 2 * n : n;
   const int g = h / p.G;
-  const int zq = sq.b * p.Hq + h, zk = sq.b * p.Hkv + g;
+  const int zq = sq.b * p.Hq + h;  // row block of the contiguous fp32 [B, Hq, S] LSE
   const int row0 = sq.start + t * C::BQ;
 
   // the warp index goes through a shuffle so the compiler knows it is warp-uniform: the warp-role
@@ -150,10 +150,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_map(&m.k);
       tma_prefetch_map(&m.v);
       mbar_expect_tx(&ctl.bar_q, C::Q_BYTES + C::DO_BYTES);
-      for (int cb = 0; cb < C::QB; ++cb) tma_load_3d(sQ + cb * (C::BQ * 128), &m.q, &ctl.bar_q, cb * 64, row0, zq);
+      for (int cb = 0; cb < C::QB; ++cb) tma_load_4d(sQ + cb * (C::BQ * 128), &m.q, &ctl.bar_q, cb * 64, row0, h, sq.b);
       if (!FWD)
         for (int cb = 0; cb < C::VB; ++cb)
-          tma_load_3d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.bar_q, cb * 64, row0, zq);
+          tma_load_4d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.bar_q, cb * 64, row0, h, sq.b);
       int issued = 0;
       for (int it = 0; it < NIT; ++it) {
         const int st = it % C::KST;
@@ -165,10 +165,10 @@ __global__ void __launch_bounds__(320, 1)
         mbar_expect_tx(&ctl.kv_full[st], C::K_BYTES + (need_v ? C::V_BYTES : 0));
         const int krow = sq.start + kt * C::BK;
         for (int cb = 0; cb < C::QB; ++cb)
-          tma_load_3d(sK + cb * (C::BK * 128), &m.k, &ctl.kv_full[st], cb * 64, krow, zk);
+          tma_load_4d(sK + cb * (C::BK * 128), &m.k, &ctl.kv_full[st], cb * 64, krow, g, sq.b);
         if (need_v)
           for (int cb = 0; cb < C::VB; ++cb)
-            tma_load_3d(sV + cb * (C::BK * 128), &m.v, &ctl.kv_full[st], cb * 64, krow, zk);
+            tma_load_4d(sV + cb * (C::BK * 128), &m.v, &ctl.kv_full[st], cb * 64, krow, g, sq.b);
         issued = it + 1;
       }
       if (ctl.abort_flag) {
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (sink2 != -INFINITY) l += ex2_approx(sink2 - mref);
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        T* o = static_cast<T*>(out) + orow * DV;
+        T* o = static_cast<T*>(out) + p.o_st.row(sq.b, h, sq.start + il);
 #pragma unroll 1
         for (int c0 = w * (DV / 2); c0 < (w + 1) * (DV / 2); c0 += 32) {
           uint32_t v[32];
@@ -413,8 +413,7 @@ __global__ void __launch_bounds__(320, 1)
       if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
         tc_fence_after();
         const bool valid = il < sq.len;
-        const size_t qrow = static_cast<size_t>(zq) * p.S + sq.start + il;
-        T* dq = static_cast<T*>(out) + qrow * DQK;
+        T* dq = static_cast<T*>(out) + p.dq_st.row(sq.b, h, sq.start + il);
 #pragma unroll 1
         for (int c0 = w * (DQK / 2); c0 < (w + 1) * (DQK / 2); c0 += 32) {
           uint32_t v[32];

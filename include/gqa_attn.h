@@ -17,10 +17,12 @@
  *       causal fused-attention backward.
  *
  * Conventions shared by every entry point
- *  - Layout: dense row-major BHSD ([P2] Description): q, dq [B,Hq,S,Dqk];
- *    k, dk [B,Hkv,S,Dqk]; v, dv [B,Hkv,S,Dv]; o, dout [B,Hq,S,Dv];
- *    lse, delta [B,Hq,S] fp32; sink, dsink [Hq] fp32.  Packed variable-length
- *    batches use B == 1, S == total tokens T and cu_seqlens ([P1] Related PRs).
+ *  - Shapes: q, dq [B,Hq,S,Dqk]; k, dk [B,Hkv,S,Dqk]; v, dv [B,Hkv,S,Dv];
+ *    o, dout [B,Hq,S,Dv]; lse, delta [B,Hq,S] fp32; sink, dsink [Hq] fp32.  By
+ *    default every tensor is dense row-major BHSD ([P2] Description); the 16-bit
+ *    ones may instead carry (batch, head, sequence) strides (gqa_stride: BSHD,
+ *    packed THD, ...).  Packed variable-length batches use B == 1, S == total
+ *    tokens T and cu_seqlens ([P1] Related PRs).
  *  - Element type of q/k/v/o/dout/dq/dk/dv: fp16 or bf16 (params.dtype).
  *    Every accumulation is fp32 ([P2] 4->2 commit: fp16 atomics fail precision).
  *  - Pointers: device pointers unless stated; base addresses of the 16-bit
@@ -79,6 +81,15 @@ typedef enum {
                           reduction alone; elsewhere plain per-thread stores. */
 } gqa_red_mode;
 
+/* Element strides of one 16-bit [B, H, S, D] tensor along batch, head and sequence; the head-dim
+ * stride is 1.  {0, 0, 0} means contiguous BHSD, i.e. {H*S*D, S*D, D}.  Otherwise every stride
+ * is a multiple of 8 elements (16 bytes), h and s are >= D, and b may be 0 only when B == 1.
+ * Examples: BSHD {S*H*D, D, H*D}; packed varlen THD with B = 1 {0, D, H*D}.  Outputs must not
+ * overlap themselves or any input. */
+typedef struct {
+  int64_t b, h, s;
+} gqa_stride;
+
 typedef struct {
   int B, Hq, Hkv;        /* batch, query heads, kv heads; Hq % Hkv == 0 (group size Hq/Hkv) */
   int S;                 /* sequence length, or total packed tokens T when cu_seqlens != NULL */
@@ -97,6 +108,10 @@ typedef struct {
   int deterministic;     /* 1: no atomics anywhere; dQ comes from a separate query-stationary
                             pass; results are bit-identical run to run; group_mode/red_mode
                             are ignored */
+  /* Memory layouts of the 16-bit tensors (zero-initialised = contiguous BHSD for all of them):
+   * inputs q, k, v, o (read by the backward preprocess, written by the forward), dout; outputs
+   * dq, dk, dv.  LSE, Delta and dsink stay contiguous fp32 [B, Hq, S] / [Hq]. */
+  gqa_stride q_st, k_st, v_st, o_st, do_st, dq_st, dk_st, dv_st;
 } gqa_attn_params;
 
 /* Bytes of workspace every call below needs for `p` (0 if `p` is invalid).  The
@@ -106,10 +121,14 @@ typedef struct {
  * may be reused across calls on the same stream. */
 size_t gqa_attn_workspace_size(const gqa_attn_params* p);
 
+/* sizeof(gqa_attn_params) as this library was compiled: bindings check their mirror of the
+ * struct against it. */
+size_t gqa_attn_params_size(void);
+
 /* Forward with causal / sliding-window / attention-sink masking ([P2] 4->2
  * commit, "flashattn_fwd: online softmax + sink + window -> O, lse").
  *   q, k, v : inputs (device, dtype).   sink : device fp32 [Hq] or NULL.
- *   o       : output [B,Hq,S,Dv] (device, dtype).
+ *   o       : output [B,Hq,S,Dv] (device, dtype), laid out as p->o_st says.
  *   lse     : output [B,Hq,S] fp32, natural log, sink included:
  *             lse_i = log(exp(sink_h) + sum_{j visible} exp(scale * q_i . k_j)). */
 gqa_status gqa_attn_fwd(const gqa_attn_params* p, const void* q, const void* k, const void* v,

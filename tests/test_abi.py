@@ -111,3 +111,34 @@ def test_strerror(lib):
         s = nat.strerror(code)
         assert s and s != "unknown status"
     assert nat.strerror(-99) == "unknown status"
+
+
+def test_params_struct_matches_library(lib):
+    # the binding refuses to load a library whose struct differs; check the numbers directly too
+    assert lib.gqa_attn_params_size() == ctypes.sizeof(nat.Params)
+
+
+def test_layout_strides_validated(lib):
+    B, H, S, D = 2, 8, 256, 64
+    bshd = (S * H * D, D, H * D)
+    assert nat.workspace_size(_p(strides={n: bshd for n in ("q", "o", "do", "dq")})) > 0
+    kv_bshd = (S * 2 * D, D, 2 * D)  # Hkv = 2
+    assert nat.workspace_size(_p(strides={"k": kv_bshd, "v": kv_bshd, "dk": kv_bshd, "dv": kv_bshd})) > 0
+    assert nat.workspace_size(_p(strides={"q": (S * H * D, D, H * D + 4)})) == 0   # not a 16-byte multiple
+    assert nat.workspace_size(_p(strides={"q": (S * H * D, 32, H * D)})) == 0      # rows closer than D
+    assert nat.workspace_size(_p(strides={"dq": (0, D, H * D)})) == 0              # batch stride 0, B > 1
+    assert nat.workspace_size(_p(B=1, strides={"dq": (0, D, H * D)})) > 0         # ... fine for B == 1
+    assert nat.workspace_size(_p(strides={"v": (S * 2 * D, -D, 2 * D)})) == 0      # negative
+
+
+def test_tensor_strides_of_common_layouts():
+    import torch
+    B, H, S, D = 2, 4, 10, 64
+    x = torch.empty(B, S, H, D).transpose(1, 2)  # BSHD view
+    assert nat.tensor_strides(x) == (S * H * D, D, H * D)
+    thd = torch.empty(S, H, D).permute(1, 0, 2).unsqueeze(0)  # packed THD as [1, H, T, D]
+    b, h, s = nat.tensor_strides(thd)
+    assert (h, s) == (D, H * D)
+    assert nat.tensor_strides(torch.empty(B, H, S, D)) == (H * S * D, S * D, D)
+    with pytest.raises(ValueError):
+        nat.tensor_strides(torch.empty(B, H, D, S).transpose(2, 3))  # head dim not contiguous
