@@ -14,20 +14,30 @@ from typing import Optional, Sequence
 import numpy as np
 
 
-def mask_matrix(S: int, causal: bool, window: int, cu_seqlens: Optional[Sequence[int]]) -> np.ndarray:
-    """allowed[i, j] for query row i and key row j."""
-    seq = np.zeros(S, dtype=np.int64)
-    if cu_seqlens is not None:
-        cu = list(cu_seqlens)
-        for s in range(len(cu) - 1):
-            seq[cu[s]:cu[s + 1]] = s
-    i = np.arange(S)[:, None]
-    j = np.arange(S)[None, :]
-    allowed = seq[:, None] == seq[None, :]
+def mask_matrix(S: int, causal: bool, window: int, cu_seqlens: Optional[Sequence[int]], Sk: Optional[int] = None,
+                cu_seqlens_k: Optional[Sequence[int]] = None) -> np.ndarray:
+    """allowed[i, j] for query row i and key row j: same sequence, and with local indices
+    il, jl and the sequence's lengths Lq, Lk, causal jl <= il + Lk - Lq, window il + Lk - Lq - jl < W."""
+    Sk = Sk or S
+    cu_q = list(cu_seqlens) if cu_seqlens is not None else [0, S]
+    cu_k = list(cu_seqlens_k) if cu_seqlens_k is not None else (list(cu_seqlens) if cu_seqlens is not None
+                                                                 else [0, Sk])
+    seq_q, loc_q, off_q = np.full(S, -1), np.zeros(S, dtype=np.int64), np.zeros(S, dtype=np.int64)
+    seq_k, loc_k = np.full(Sk, -2), np.zeros(Sk, dtype=np.int64)
+    for s in range(len(cu_q) - 1):
+        lq, lk = cu_q[s + 1] - cu_q[s], cu_k[s + 1] - cu_k[s]
+        seq_q[cu_q[s]:cu_q[s + 1]] = s
+        loc_q[cu_q[s]:cu_q[s + 1]] = np.arange(lq)
+        off_q[cu_q[s]:cu_q[s + 1]] = lk - lq
+        seq_k[cu_k[s]:cu_k[s + 1]] = s
+        loc_k[cu_k[s]:cu_k[s + 1]] = np.arange(lk)
+    diag = (loc_q + off_q)[:, None]  # each query's key diagonal
+    jl = loc_k[None, :]
+    allowed = seq_q[:, None] == seq_k[None, :]
     if causal:
-        allowed &= j <= i
+        allowed &= jl <= diag
     if window > 0:
-        allowed &= (i - j) < window
+        allowed &= (diag - jl) < window
     return allowed
 
 
@@ -40,10 +50,13 @@ def mha_head(q, k, v, dout, scale, allowed, sink: Optional[float]):
     S = np.where(allowed, S, -np.inf)
     cols = S if sink is None else np.concatenate([S, np.full((S.shape[0], 1), sink)], axis=1)
     m = cols.max(axis=1, keepdims=True)
+    empty = ~np.isfinite(m)                      # a query row that sees nothing (no key, no sink)
+    m = np.where(empty, 0.0, m)
     e = np.exp(cols - m)
     z = e.sum(axis=1, keepdims=True)
-    lse = (m + np.log(z))[:, 0]
-    probs = e / z
+    with np.errstate(divide="ignore"):
+        lse = (m + np.log(z))[:, 0]
+    probs = np.where(z > 0, e / np.where(z > 0, z, 1.0), 0.0)
     P = probs[:, :S.shape[1]]
     p_sink = probs[:, S.shape[1]] if sink is not None else np.zeros(S.shape[0])
     O = P @ v
@@ -57,16 +70,17 @@ def mha_head(q, k, v, dout, scale, allowed, sink: Optional[float]):
     return dict(O=O, LSE=lse, P=P, p_sink=p_sink, dP=dP, dS=dS, Delta=Delta, dQ=dQ, dK=dK, dV=dV, dsink=dsink)
 
 
-def gqa(q, k, v, dout, scale, causal=True, window=0, cu_seqlens=None, sink=None):
-    """Full GQA forward+backward for [B,H,S,D] float64 arrays via per-head MHA."""
+def gqa(q, k, v, dout, scale, causal=True, window=0, cu_seqlens=None, sink=None, cu_seqlens_k=None):
+    """Full GQA forward+backward for [B,H,S,D] float64 arrays via per-head MHA (k, v may have
+    another length Sk)."""
     B, Hq, S, _ = q.shape
-    Hkv = k.shape[1]
+    Hkv, Sk = k.shape[1], k.shape[2]
     G = Hq // Hkv
-    allowed = mask_matrix(S, causal, window, cu_seqlens)
+    allowed = mask_matrix(S, causal, window, cu_seqlens, Sk, cu_seqlens_k)
     out = dict(
         o=np.zeros((B, Hq, S, v.shape[3])), lse=np.zeros((B, Hq, S)), delta=np.zeros((B, Hq, S)),
         dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v), dsink=np.zeros(Hq),
-        P=np.zeros((B, Hq, S, S)), dS=np.zeros((B, Hq, S, S)), dP=np.zeros((B, Hq, S, S)),
+        P=np.zeros((B, Hq, S, Sk)), dS=np.zeros((B, Hq, S, Sk)), dP=np.zeros((B, Hq, S, Sk)),
         p_sink=np.zeros((B, Hq, S)),
     )
     for b in range(B):

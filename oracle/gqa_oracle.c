@@ -9,8 +9,11 @@
  *
  *   g          = h / (Hq / Hkv)                        ("bx // groups", tilelang
  *                                                       PR #1093, Additional comments)
- *   A(i)       = { j in the same sequence as i, j <= i if causal,
- *                  i - j < W if a window W > 0 is set }
+ *   A(i)       = { j in the same sequence as i, j <= i + (Lk - Lq) if causal,
+ *                  i + (Lk - Lq) - j < W if a window W > 0 is set }
+ *                with i, j local to their sequence, Lq / Lk its query / key lengths:
+ *                the causal diagonal is aligned at the bottom right (the last query sees
+ *                the last key), which is the top-left j <= i when Lq == Lk
  *   S_ij       = scale * sum_d Q[h,i,d] K[g,j,d]       (tilelang-ascend PR #1638,
  *                                                       review thread, k1/k2)
  *   LSE_i      = log( [e^{sink_h}] + sum_{j in A(i)} e^{S_ij} )
@@ -32,7 +35,8 @@
  *
  * Layout: every tensor is dense row-major [B, H, S, D] in fp64 (S is the
  * per-batch length, or the packed token count T when cu_seqlens is given, in
- * which case B == 1).  LSE / Delta are [B, Hq, S].
+ * which case B == 1); k, v, dk, dv have Sk rows per (b, h) instead (Sk = S
+ * unless set).  LSE / Delta are [B, Hq, S].
  *
  * Evaluation order is the plain definition: a row pass over (b, h, i) and a
  * column pass over (b, g, j) that revisits every (h, i) which sees key j, so no
@@ -51,26 +55,34 @@ typedef struct {
   int nseq;            /* number of packed sequences when cu_seqlens != NULL */
   const int32_t* cu_seqlens; /* [nseq+1] token offsets, or NULL (dense) */
   const double* sink;  /* [Hq] or NULL */
+  int Sk;              /* key rows per batch (or packed key tokens); 0: the same as S */
+  const int32_t* cu_seqlens_k; /* [nseq+1] key offsets, or NULL: the same as cu_seqlens */
 } oracle_problem;
+
+static inline int key_len(const oracle_problem* p) { return p->Sk > 0 ? p->Sk : p->S; }
 
 /* Range of key rows visible to query row i (both in absolute token index
  * within the S axis), returned as [lo, hi) ; empty if lo >= hi. */
 static void key_range(const oracle_problem* p, int i, int* lo, int* hi) {
-  int s0 = 0, s1 = p->S;
+  int qs = 0, ql = p->S, ks = 0, kl = key_len(p);
   if (p->cu_seqlens) {
+    const int32_t* ck = p->cu_seqlens_k ? p->cu_seqlens_k : p->cu_seqlens;
     for (int s = 0; s < p->nseq; ++s) {
       if (i >= p->cu_seqlens[s] && i < p->cu_seqlens[s + 1]) {
-        s0 = p->cu_seqlens[s];
-        s1 = p->cu_seqlens[s + 1];
+        qs = p->cu_seqlens[s];
+        ql = p->cu_seqlens[s + 1] - qs;
+        ks = ck[s];
+        kl = ck[s + 1] - ks;
         break;
       }
     }
   }
-  int a = s0, b = s1;
-  if (p->causal && i + 1 < b) b = i + 1;
-  if (p->window > 0 && i - p->window + 1 > a) a = i - p->window + 1;
-  *lo = a;
-  *hi = b;
+  const int il = i - qs, off = kl - ql;  /* query il sits on key diagonal il + off */
+  int a = 0, b = kl;
+  if (p->causal && il + off + 1 < b) b = il + off + 1;
+  if (p->window > 0 && il + off - p->window + 1 > a) a = il + off - p->window + 1;
+  *lo = ks + a;
+  *hi = ks + b;  /* empty when b <= a */
 }
 
 static inline const double* row(const double* t, int H, int S, int D, int b, int h, int i) {
@@ -86,7 +98,7 @@ static double dot(const double* x, const double* y, int n) {
 /* Scaled logit S_ij. */
 static double logit(const oracle_problem* p, const double* q, const double* k, int b, int h, int i, int j) {
   const int g = h / (p->Hq / p->Hkv);
-  return p->scale * dot(row(q, p->Hq, p->S, p->Dqk, b, h, i), row(k, p->Hkv, p->S, p->Dqk, b, g, j), p->Dqk);
+  return p->scale * dot(row(q, p->Hq, p->S, p->Dqk, b, h, i), row(k, p->Hkv, key_len(p), p->Dqk, b, g, j), p->Dqk);
 }
 
 /* LSE_i from its definition, with the row maximum subtracted for stability. */
@@ -122,7 +134,7 @@ void oracle_forward(const oracle_problem* p, const double* q, const double* k, c
     key_range(p, i, &lo, &hi);
     for (int j = lo; j < hi; ++j) {
       const double pij = exp(logit(p, q, k, b, h, i, j) - L);
-      const double* vj = row(v, p->Hkv, p->S, p->Dv, b, g, j);
+      const double* vj = row(v, p->Hkv, key_len(p), p->Dv, b, g, j);
       for (int d = 0; d < p->Dv; ++d) orow[d] += pij * vj[d];
     }
   }
@@ -140,7 +152,7 @@ static double grad_logit(const oracle_problem* p, const double* q, const double*
                          const double* dout, double L, double D_i, int b, int h, int i, int j, double* pij_out) {
   const int g = h / (p->Hq / p->Hkv);
   const double pij = exp(logit(p, q, k, b, h, i, j) - L);
-  const double dpij = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), row(v, p->Hkv, p->S, p->Dv, b, g, j), p->Dv);
+  const double dpij = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), row(v, p->Hkv, key_len(p), p->Dv, b, g, j), p->Dv);
   if (pij_out) *pij_out = pij;
   return pij * (dpij - D_i) * p->scale;
 }
@@ -148,7 +160,7 @@ static double grad_logit(const oracle_problem* p, const double* q, const double*
 /*
  * Backward.  Inputs: q, k, v, dout, and the forward's lse and o (Delta is
  * formed from o and dout).  Outputs: delta [B,Hq,S], dq [B,Hq,S,Dqk],
- * dk [B,Hkv,S,Dqk], dv [B,Hkv,S,Dv], dsink [Hq] (only if p->sink).
+ * dk [B,Hkv,Sk,Dqk], dv [B,Hkv,Sk,Dv], dsink [Hq] (only if p->sink).
  */
 void oracle_backward(const oracle_problem* p, const double* q, const double* k, const double* v,
                      const double* o, const double* lse, const double* dout, double* delta, double* dq,
@@ -168,16 +180,17 @@ void oracle_backward(const oracle_problem* p, const double* q, const double* k, 
     key_range(p, i, &lo, &hi);
     for (int j = lo; j < hi; ++j) {
       const double ds = grad_logit(p, q, k, v, dout, lse[r], delta[r], b, h, i, j, NULL);
-      const double* kj = row(k, p->Hkv, p->S, p->Dqk, b, g, j);
+      const double* kj = row(k, p->Hkv, key_len(p), p->Dqk, b, g, j);
       for (int d = 0; d < p->Dqk; ++d) dqi[d] += ds * kj[d];
     }
   }
 
   /* column pass: dK_j, dV_j summed over every query head of the group */
-  const long ncols = (long)p->B * p->Hkv * p->S;
+  const int SK = key_len(p);
+  const long ncols = (long)p->B * p->Hkv * SK;
 #pragma omp parallel for schedule(dynamic, 16)
   for (long c = 0; c < ncols; ++c) {
-    const int j = (int)(c % p->S), g = (int)((c / p->S) % p->Hkv), b = (int)(c / ((long)p->S * p->Hkv));
+    const int j = (int)(c % SK), g = (int)((c / SK) % p->Hkv), b = (int)(c / ((long)SK * p->Hkv));
     double* dkj = dk + (size_t)c * p->Dqk;
     double* dvj = dv + (size_t)c * p->Dv;
     for (int d = 0; d < p->Dqk; ++d) dkj[d] = 0.0;
@@ -237,7 +250,7 @@ void oracle_sample_rows(const oracle_problem* p, const double* q, const double* 
     key_range(p, i, &lo, &hi);
     for (int j = lo; j < hi; ++j) {
       const double pij = exp(logit(p, q, k, b, h, i, j) - L);
-      const double* vj = row(v, p->Hkv, p->S, p->Dv, b, g, j);
+      const double* vj = row(v, p->Hkv, key_len(p), p->Dv, b, g, j);
       for (int d = 0; d < p->Dv; ++d) orow[d] += pij * vj[d];
     }
     const double Di = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), orow, p->Dv);
@@ -247,7 +260,7 @@ void oracle_sample_rows(const oracle_problem* p, const double* q, const double* 
     for (int d = 0; d < p->Dqk; ++d) dqi[d] = 0.0;
     for (int j = lo; j < hi; ++j) {
       const double ds = grad_logit(p, q, k, v, dout, L, Di, b, h, i, j, NULL);
-      const double* kj = row(k, p->Hkv, p->S, p->Dqk, b, g, j);
+      const double* kj = row(k, p->Hkv, key_len(p), p->Dqk, b, g, j);
       for (int d = 0; d < p->Dqk; ++d) dqi[d] += ds * kj[d];
     }
   }
@@ -275,7 +288,7 @@ void oracle_sample_cols(const oracle_problem* p, const double* q, const double* 
         for (int d = 0; d < p->Dv; ++d) orow[d] = 0.0;
         for (int jj = lo; jj < hi; ++jj) {
           const double pw = exp(logit(p, q, k, b, h, i, jj) - L);
-          const double* vj = row(v, p->Hkv, p->S, p->Dv, b, g, jj);
+          const double* vj = row(v, p->Hkv, key_len(p), p->Dv, b, g, jj);
           for (int d = 0; d < p->Dv; ++d) orow[d] += pw * vj[d];
         }
         const double Di = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), orow, p->Dv);

@@ -40,6 +40,7 @@ class _Problem(ctypes.Structure):
         ("Dqk", ctypes.c_int), ("Dv", ctypes.c_int), ("causal", ctypes.c_int), ("window", ctypes.c_int),
         ("scale", ctypes.c_double), ("nseq", ctypes.c_int),
         ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)), ("sink", ctypes.POINTER(ctypes.c_double)),
+        ("Sk", ctypes.c_int), ("cu_seqlens_k", ctypes.POINTER(ctypes.c_int32)),
     ]
 
 
@@ -63,7 +64,10 @@ def _load():
 
 @dataclass
 class Problem:
-    """Shapes and masking of one attention problem (layout [B, H, S, D])."""
+    """Shapes and masking of one attention problem (layout [B, H, S, D]; k / v have Sk rows).
+
+    With Sk != S (or key offsets cu_seqlens_k different from cu_seqlens) the causal diagonal
+    is aligned at the bottom right: query i of a sequence sees key j iff j <= i + (Lk - Lq)."""
     B: int
     Hq: int
     Hkv: int
@@ -74,9 +78,15 @@ class Problem:
     window: int = 0
     scale: Optional[float] = None
     cu_seqlens: Optional[Sequence[int]] = None
+    Sk: Optional[int] = None
+    cu_seqlens_k: Optional[Sequence[int]] = None
 
     def resolved_scale(self) -> float:
         return float(self.scale) if self.scale is not None else 1.0 / np.sqrt(self.Dqk)
+
+    @property
+    def key_len(self) -> int:
+        return int(self.Sk) if self.Sk else int(self.S)
 
 
 def _dp(a: np.ndarray):
@@ -109,6 +119,13 @@ def _mk(pb: Problem, sink: Optional[np.ndarray], keep: list):
         st.sink = _dp(s)
     else:
         st.sink = ctypes.POINTER(ctypes.c_double)()
+    st.Sk = pb.key_len
+    if pb.cu_seqlens_k is not None:
+        ck = np.ascontiguousarray(np.asarray(pb.cu_seqlens_k, dtype=np.int32))
+        keep.append(ck)
+        st.cu_seqlens_k = _ip(ck)
+    else:
+        st.cu_seqlens_k = ctypes.POINTER(ctypes.c_int32)()
     return st
 
 
@@ -134,8 +151,8 @@ def backward(pb: Problem, q, k, v, o, lse, dout, sink=None):
     st = _mk(pb, sink, keep)
     delta = np.zeros((pb.B, pb.Hq, pb.S))
     dq = np.zeros((pb.B, pb.Hq, pb.S, pb.Dqk))
-    dk = np.zeros((pb.B, pb.Hkv, pb.S, pb.Dqk))
-    dv = np.zeros((pb.B, pb.Hkv, pb.S, pb.Dv))
+    dk = np.zeros((pb.B, pb.Hkv, pb.key_len, pb.Dqk))
+    dv = np.zeros((pb.B, pb.Hkv, pb.key_len, pb.Dv))
     dsink = np.zeros(pb.Hq)
     lib.oracle_backward(ctypes.byref(st), _dp(q), _dp(k), _dp(v), _dp(o), _dp(lse), _dp(dout), _dp(delta),
                         _dp(dq), _dp(dk), _dp(dv), _dp(dsink))

@@ -32,8 +32,8 @@ def _rand(shape, rng, std=1.0):
 def _inputs(pb, seed=0, with_sink=False):
     rng = np.random.default_rng(seed)
     q = _rand((pb.B, pb.Hq, pb.S, pb.Dqk), rng)
-    k = _rand((pb.B, pb.Hkv, pb.S, pb.Dqk), rng)
-    v = _rand((pb.B, pb.Hkv, pb.S, pb.Dv), rng)
+    k = _rand((pb.B, pb.Hkv, pb.key_len, pb.Dqk), rng)
+    v = _rand((pb.B, pb.Hkv, pb.key_len, pb.Dv), rng)
     do = _rand((pb.B, pb.Hq, pb.S, pb.Dv), rng)
     sink = _rand((pb.Hq,), rng) if with_sink else None
     return q, k, v, do, sink
@@ -241,3 +241,128 @@ def test_empty_sequence_rows_are_untouched():
     o1, l1 = orc.forward(pb1, q, k, v)
     o2, l2 = orc.forward(pb2, q, k, v)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- Sq != Sk (bottom-right causal)
+# query i of a sequence with Lq queries and Lk keys sees key j iff j <= i + (Lk - Lq) (causal) and
+# i + (Lk - Lq) - j < W (window): the last query sees the last key.
+
+def _cross_cases():
+    return [
+        dict(S=5, Sk=8, causal=True, window=0, sink=False, cu=None, cuk=None),   # chunked prefill
+        dict(S=5, Sk=8, causal=True, window=3, sink=True, cu=None, cuk=None),
+        dict(S=8, Sk=5, causal=True, window=0, sink=False, cu=None, cuk=None),   # 3 rows see nothing
+        dict(S=8, Sk=5, causal=True, window=0, sink=True, cu=None, cuk=None),
+        dict(S=4, Sk=7, causal=False, window=0, sink=True, cu=None, cuk=None),   # cross-attention
+        dict(S=7, Sk=7, causal=True, window=0, sink=False, cu=[0, 3, 7], cuk=[0, 5, 7]),  # per-sequence offsets
+    ]
+
+
+def _cross_pb(c, **shape):
+    shp = dict(TINY, S=c["S"])
+    shp.update(shape)
+    return orc.Problem(causal=c["causal"], window=c["window"], scale=0.7, cu_seqlens=c["cu"], Sk=c["Sk"],
+                       cu_seqlens_k=c["cuk"], **shp)
+
+
+def _cross_id(c):
+    return f"q{c['S']}k{c['Sk']}c{int(c['causal'])}w{c['window']}s{int(c['sink'])}{'v' if c['cu'] else ''}"
+
+
+@pytest.mark.parametrize("case", _cross_cases(), ids=_cross_id)
+def test_cross_lengths_finite_differences(case):
+    pb = _cross_pb(case)
+    q, k, v, do, sink = _inputs(pb, seed=13, with_sink=case["sink"])
+    o, lse = orc.forward(pb, q, k, v, sink)
+    g = orc.backward(pb, q, k, v, o, lse, do, sink)
+    h = 1e-5
+
+    def fd(x):
+        num = np.zeros_like(x)
+        flat, nflat = x.reshape(-1), num.reshape(-1)
+        for t in range(flat.size):
+            keep = flat[t]
+            flat[t] = keep + h
+            lp = _loss(pb, q, k, v, do, sink)
+            flat[t] = keep - h
+            lm = _loss(pb, q, k, v, do, sink)
+            flat[t] = keep
+            nflat[t] = (lp - lm) / (2 * h)
+        return num
+
+    for name, x in (("dq", q), ("dk", k), ("dv", v)):
+        num = fd(x)
+        assert np.abs(num - g[name]).max() <= 1e-7 * max(1.0, np.abs(num).max()), name
+    if sink is not None:
+        num = fd(sink)
+        assert np.abs(num - g["dsink"]).max() <= 1e-7 * max(1.0, np.abs(num).max())
+
+
+@pytest.mark.parametrize("case", _cross_cases(), ids=_cross_id)
+def test_cross_lengths_against_bruteforce(case):
+    pb = _cross_pb(case)
+    q, k, v, do, sink = _inputs(pb, seed=17, with_sink=case["sink"])
+    o, lse = orc.forward(pb, q, k, v, sink)
+    g = orc.backward(pb, q, k, v, o, lse, do, sink)
+    r = brute.gqa(q, k, v, do, pb.resolved_scale(), causal=pb.causal, window=pb.window, cu_seqlens=pb.cu_seqlens,
+                  sink=sink, cu_seqlens_k=pb.cu_seqlens_k)
+    np.testing.assert_allclose(o, r["o"], rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(r["lse"]))
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(lse[fin], r["lse"][fin], rtol=0, atol=1e-12)
+    for name in ("delta", "dq", "dk", "dv"):
+        np.testing.assert_allclose(g[name], r[name], rtol=0, atol=1e-12, err_msg=name)
+
+
+@pytest.mark.parametrize("case", _cross_cases(), ids=_cross_id)
+def test_cross_lengths_against_torch_autograd(case):
+    pb = _cross_pb(case, Hq=6, Hkv=3, Dqk=6, Dv=4)
+    q, k, v, do, sink = _inputs(pb, seed=23, with_sink=case["sink"])
+    o, lse = orc.forward(pb, q, k, v, sink)
+    g = orc.backward(pb, q, k, v, o, lse, do, sink)
+    G = pb.Hq // pb.Hkv
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    ts = torch.tensor(sink, requires_grad=True) if sink is not None else None
+    allowed = torch.tensor(brute.mask_matrix(pb.S, pb.causal, pb.window, pb.cu_seqlens, pb.key_len,
+                                             pb.cu_seqlens_k))
+    logits = torch.einsum("bhid,bhjd->bhij", tq, tk.repeat_interleave(G, dim=1)) * pb.resolved_scale()
+    logits = logits.masked_fill(~allowed, float("-inf"))
+    if ts is not None:
+        logits = torch.cat([logits, ts.view(1, pb.Hq, 1, 1).expand(pb.B, pb.Hq, pb.S, 1)], dim=-1)
+    probs = torch.nan_to_num(torch.softmax(logits, dim=-1))[..., :pb.key_len]  # rows that see nothing: 0
+    out = probs @ tv.repeat_interleave(G, dim=1)
+    (out * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(o, out.detach().numpy(), rtol=0, atol=1e-12)
+    for name, t in (("dq", tq), ("dk", tk), ("dv", tv)) + ((("dsink", ts),) if ts is not None else ()):
+        np.testing.assert_allclose(g[name], t.grad.numpy(), rtol=0, atol=1e-11, err_msg=name)
+
+
+def test_decode_row_sees_every_key():
+    """One query against Sk keys, causal bottom-right: it sees all of them, i.e. plain
+    non-causal attention."""
+    a = orc.Problem(B=1, Hq=4, Hkv=2, S=1, Dqk=5, Dv=3, causal=True, scale=0.7, Sk=9)
+    b = orc.Problem(B=1, Hq=4, Hkv=2, S=1, Dqk=5, Dv=3, causal=False, scale=0.7, Sk=9)
+    q, k, v, do, _ = _inputs(a, seed=3)
+    oa, la = orc.forward(a, q, k, v)
+    ob, lb = orc.forward(b, q, k, v)
+    np.testing.assert_array_equal(oa, ob)
+    np.testing.assert_array_equal(la, lb)
+    ga, gb = orc.backward(a, q, k, v, oa, la, do), orc.backward(b, q, k, v, ob, lb, do)
+    for n in ("dq", "dk", "dv"):
+        np.testing.assert_array_equal(ga[n], gb[n])
+
+
+def test_rows_without_keys():
+    """More queries than keys, causal: the first S - Sk query rows see no key; without a sink
+    their O and dQ are zero, LSE is -inf and they add nothing to dK / dV."""
+    pb = orc.Problem(B=1, Hq=2, Hkv=1, S=8, Dqk=5, Dv=3, causal=True, scale=0.7, Sk=5)
+    q, k, v, do, _ = _inputs(pb, seed=9)
+    o, lse = orc.forward(pb, q, k, v)
+    g = orc.backward(pb, q, k, v, o, lse, do)
+    assert np.all(o[:, :, :3] == 0) and np.all(np.isneginf(lse[:, :, :3])) and np.all(np.isfinite(lse[:, :, 3:]))
+    assert np.all(g["dq"][:, :, :3] == 0)
+    do2 = do.copy()
+    do2[:, :, :3] = 123.0  # the gradient of those rows cannot reach K or V
+    g2 = orc.backward(pb, q, k, v, o, lse, do2)
+    np.testing.assert_array_equal(g["dk"], g2["dk"])
+    np.testing.assert_array_equal(g["dv"], g2["dv"])
