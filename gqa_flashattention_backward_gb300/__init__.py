@@ -40,8 +40,9 @@ def preferred_red_mode(Dqk: int) -> int:
 
 
 def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=GQA_GROUP_TMEM,
-            red_mode=None, deterministic=False, **tensors):
-    """`tensors`: any of o, do, dq, dk, dv whose layouts the call uses."""
+            red_mode=None, deterministic=False, cu_seqlens_k=None, max_seqlen_k=None, **tensors):
+    """`tensors`: any of o, do, dq, dk, dv whose layouts the call uses.  k / v may have another
+    length than q (k.shape[2]): the causal diagonal is then aligned at the bottom right."""
     B, Hq, S, Dqk = q.shape
     if red_mode is None:
         red_mode = preferred_red_mode(Dqk)
@@ -53,7 +54,8 @@ def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=G
     strides = {n: native.tensor_strides(t) for n, t in named.items()}
     return native.make_params(B, Hq, Hkv, S, Dqk, Dv, q.dtype, causal=causal, window=window, scale=scale,
                               cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, group_mode=group_mode,
-                              red_mode=red_mode, deterministic=deterministic, strides=strides)
+                              red_mode=red_mode, deterministic=deterministic, strides=strides, Sk=k.shape[2],
+                              cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k)
 
 
 def _empty_like_layout(ref: torch.Tensor, last_dim: int) -> torch.Tensor:
@@ -68,11 +70,13 @@ def _empty_like_layout(ref: torch.Tensor, last_dim: int) -> torch.Tensor:
 def attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = True, window: int = 0,
                       scale: Optional[float] = None, sink: Optional[torch.Tensor] = None,
                       cu_seqlens: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
+                      cu_seqlens_k: Optional[torch.Tensor] = None, max_seqlen_k: Optional[int] = None,
                       workspace: Optional[torch.Tensor] = None):
     """Returns (o, lse): o [B,Hq,S,Dv] in q's dtype, lse [B,Hq,S] fp32 (natural log, sink included)."""
     B, Hq, S, _ = q.shape
     o = _empty_like_layout(q, v.shape[3])
-    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, o=o)
+    p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, cu_seqlens_k=cu_seqlens_k,
+                max_seqlen_k=max_seqlen_k, o=o)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     ws = workspace if workspace is not None else native.alloc_workspace(p, q.device)
     native.fwd(p, q, k, v, sink, o, lse, ws)
@@ -84,6 +88,7 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                        sink: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
                        max_seqlen: Optional[int] = None, group_mode: int = GQA_GROUP_TMEM,
                        red_mode: Optional[int] = None, deterministic: bool = False,
+                       cu_seqlens_k: Optional[torch.Tensor] = None, max_seqlen_k: Optional[int] = None,
                        workspace: Optional[torch.Tensor] = None, out: Optional[dict] = None) -> dict:
     """Returns dict(dq, dk, dv, delta[, dsink]).  `out` may hold preallocated tensors of the same names.
     red_mode None picks :func:`preferred_red_mode`."""
@@ -98,7 +103,8 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
     if "dv" not in res:
         res["dv"] = _empty_like_layout(v, Dv)
     p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode, red_mode, deterministic,
-                o=o, do=dout, dq=res["dq"], dk=res["dk"], dv=res["dv"])
+                cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, o=o, do=dout, dq=res["dq"], dk=res["dk"],
+                dv=res["dv"])
     if "delta" not in res:
         res["delta"] = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
     if sink is not None and "dsink" not in res:
@@ -117,12 +123,14 @@ class GqaAttentionFunction(torch.autograd.Function):
     backward entry points on them.  Every step runs in the CUDA library."""
 
     @staticmethod
-    def forward(ctx, q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic):
+    def forward(ctx, q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic, cu_seqlens_k=None,
+                max_seqlen_k=None):
         o, lse = attention_forward(q, k, v, causal=causal, window=window, scale=scale, sink=sink,
-                                   cu_seqlens=cu_seqlens, max_seqlen=max_seqlen)
+                                   cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, cu_seqlens_k=cu_seqlens_k,
+                                   max_seqlen_k=max_seqlen_k)
         ctx.save_for_backward(q, k, v, o, lse, sink)
         ctx.opts = dict(causal=causal, window=window, scale=scale, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
-                        deterministic=deterministic)
+                        deterministic=deterministic, cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k)
         return o
 
     @staticmethod
@@ -130,13 +138,15 @@ class GqaAttentionFunction(torch.autograd.Function):
         q, k, v, o, lse, sink = ctx.saved_tensors
         g = attention_backward(q, k, v, o, lse, do.contiguous(), sink=sink, **ctx.opts)
         dsink = g.get("dsink") if sink is not None and ctx.needs_input_grad[3] else None
-        return g["dq"], g["dk"], g["dv"], dsink, None, None, None, None, None, None
+        return g["dq"], g["dk"], g["dv"], dsink, None, None, None, None, None, None, None, None
 
 
 def gqa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = True, window: int = 0,
                   scale: Optional[float] = None, sink: Optional[torch.Tensor] = None,
                   cu_seqlens: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
-                  deterministic: bool = False) -> torch.Tensor:
+                  deterministic: bool = False, cu_seqlens_k: Optional[torch.Tensor] = None,
+                  max_seqlen_k: Optional[int] = None) -> torch.Tensor:
     """Differentiable grouped-query attention: returns O [B,Hq,S,Dv]; ``O.backward(dO)`` fills
     q.grad, k.grad, v.grad (and sink.grad, fp32) through the backward kernels."""
-    return GqaAttentionFunction.apply(q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic)
+    return GqaAttentionFunction.apply(q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic,
+                                      cu_seqlens_k, max_seqlen_k)

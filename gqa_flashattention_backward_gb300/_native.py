@@ -56,7 +56,9 @@ class Params(ctypes.Structure):
         ("window", ctypes.c_int), ("scale", ctypes.c_float), ("cu_seqlens", ctypes.c_void_p),
         ("nseq", ctypes.c_int), ("max_seqlen", ctypes.c_int), ("group_mode", ctypes.c_int),
         ("red_mode", ctypes.c_int), ("deterministic", ctypes.c_int),
-    ] + [(n, Stride) for n in STRIDE_FIELDS]
+    ] + [(n, Stride) for n in STRIDE_FIELDS] + [
+        ("Sk", ctypes.c_int), ("cu_seqlens_k", ctypes.c_void_p), ("max_seqlen_k", ctypes.c_int),
+    ]
 
 
 _lib = None
@@ -128,7 +130,7 @@ def _check(status: int, what: str):
 
 def make_params(B, Hq, Hkv, S, Dqk, Dv, dtype, causal=True, window=0, scale=None, cu_seqlens=None,
                 max_seqlen=None, group_mode=GQA_GROUP_TMEM, red_mode=GQA_RED_V4, deterministic=False,
-                strides=None) -> Params:
+                strides=None, Sk=None, cu_seqlens_k=None, max_seqlen_k=None) -> Params:
     """Build the parameter struct.  `dtype` is a torch dtype (float16/bfloat16);
     `cu_seqlens` a device int32 tensor or None; `strides` maps some of "q", "k", "v", "o", "do",
     "dq", "dk", "dv" to (batch, head, sequence) element strides (missing: contiguous BHSD)."""
@@ -149,6 +151,9 @@ def make_params(B, Hq, Hkv, S, Dqk, Dv, dtype, causal=True, window=0, scale=None
     p.group_mode = int(group_mode)
     p.red_mode = int(red_mode)
     p.deterministic = int(bool(deterministic))
+    p.Sk = int(Sk) if Sk is not None and int(Sk) != int(S) else 0
+    p.cu_seqlens_k = cu_seqlens_k.data_ptr() if cu_seqlens_k is not None else None
+    p.max_seqlen_k = int(max_seqlen_k) if max_seqlen_k is not None else 0
     for name, st in (strides or {}).items():
         s = getattr(p, name + "_st")
         s.b, s.h, s.s = (int(x) for x in st)

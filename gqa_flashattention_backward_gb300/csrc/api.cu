@@ -81,6 +81,9 @@ gqa_status validate(const gqa_attn_params* p) {
   if (p->causal != 0 && p->causal != 1) return GQA_ERR_INVALID_ARG;
   if (p->window > 0 && !p->causal) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(p->scale) || !(p->scale > 0.f)) return GQA_ERR_INVALID_ARG;
+  if (p->Sk < 0 || p->max_seqlen_k < 0) return GQA_ERR_INVALID_ARG;
+  if (p->cu_seqlens_k && !p->cu_seqlens) return GQA_ERR_INVALID_ARG;
+  if (p->cu_seqlens && !p->cu_seqlens_k && p->Sk != 0 && p->Sk != p->S) return GQA_ERR_INVALID_ARG;
   if (p->S > 0 && (!valid_stride(p->q_st, p->B, p->Dqk) || !valid_stride(p->k_st, p->B, p->Dqk) ||
       !valid_stride(p->v_st, p->B, p->Dv) || !valid_stride(p->o_st, p->B, p->Dv) ||
       !valid_stride(p->do_st, p->B, p->Dv) || !valid_stride(p->dq_st, p->B, p->Dqk) ||
@@ -96,8 +99,15 @@ gqa_status validate(const gqa_attn_params* p) {
   } else if (p->B > 65535) {
     return GQA_ERR_INVALID_ARG;
   }
+  if (p->cu_seqlens_k) {
+    const int sk = p->Sk > 0 ? p->Sk : p->S;
+    if (!aligned(p->cu_seqlens_k, 4) || p->max_seqlen_k < 0 || (sk > 0 && p->max_seqlen_k > sk))
+      return GQA_ERR_INVALID_ARG;
+  }
   const long long max_len = p->cu_seqlens ? p->max_seqlen : p->S;
-  if ((max_len + 127) / 128 > 65535) return GQA_ERR_UNSUPPORTED;
+  const long long max_len_k = p->cu_seqlens ? (p->cu_seqlens_k && p->max_seqlen_k > 0 ? p->max_seqlen_k : max_len)
+                                            : (p->Sk > 0 ? p->Sk : p->S);
+  if ((max_len + 127) / 128 > 65535 || (max_len_k + 127) / 128 > 65535) return GQA_ERR_UNSUPPORTED;
   if (!supported_dims(p->Dqk, p->Dv)) return GQA_ERR_UNSUPPORTED;
   // bulk dQ reduction needs shared-memory staging, which only the d=64 tile has room for
   if (!p->deterministic && p->red_mode == GQA_RED_BULK && kv_kernel_has_dq(p->Dqk) && !kv_kernel_has_bulk_dq(p->Dqk))
@@ -134,16 +144,19 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   pr.max_len = p->cu_seqlens ? p->max_seqlen : p->S;
   pr.ntiles = (pr.max_len + kStatTile - 1) / kStatTile;
   pr.wait_limit = g_wait_limit.load();
+  pr.Sk = p->Sk > 0 ? p->Sk : p->S;
+  pr.cu_seqlens_k = p->cu_seqlens ? p->cu_seqlens_k : nullptr;
+  pr.max_len_k = p->cu_seqlens ? (p->cu_seqlens_k && p->max_seqlen_k > 0 ? p->max_seqlen_k : pr.max_len) : pr.Sk;
   pr.q_st = resolve(p->q_st, p->B, p->Hq, p->S, p->Dqk);
-  pr.k_st = resolve(p->k_st, p->B, p->Hkv, p->S, p->Dqk);
-  pr.v_st = resolve(p->v_st, p->B, p->Hkv, p->S, p->Dv);
+  pr.k_st = resolve(p->k_st, p->B, p->Hkv, pr.Sk, p->Dqk);
+  pr.v_st = resolve(p->v_st, p->B, p->Hkv, pr.Sk, p->Dv);
   pr.o_st = resolve(p->o_st, p->B, p->Hq, p->S, p->Dv);
   pr.do_st = resolve(p->do_st, p->B, p->Hq, p->S, p->Dv);
   pr.dq_st = resolve(p->dq_st, p->B, p->Hq, p->S, p->Dqk);
-  pr.dk_st = resolve(p->dk_st, p->B, p->Hkv, p->S, p->Dqk);
-  pr.dv_st = resolve(p->dv_st, p->B, p->Hkv, p->S, p->Dv);
-  d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc, d.need_dkdv_acc,
-                   d.need_fold);
+  pr.dk_st = resolve(p->dk_st, p->B, p->Hkv, pr.Sk, p->Dqk);
+  pr.dv_st = resolve(p->dv_st, p->B, p->Hkv, pr.Sk, p->Dv);
+  d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Sk, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc,
+                   d.need_dkdv_acc, d.need_fold);
   uint8_t* base = static_cast<uint8_t*>(ws);
   pr.err = reinterpret_cast<int*>(base + d.ws.err_off);
   pr.nlse2 = reinterpret_cast<float*>(base + d.ws.lse2_off);
@@ -218,8 +231,8 @@ gqa_status gqa_attn_fwd(const gqa_attn_params* p, const void* q, const void* k, 
   Maps m;
   std::memset(&m, 0, sizeof(m));
   const int bk = q_kernel_bk();
-  if (!map16(&m.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, 128, bf) || !map16(&m.k, k, p->Dqk, p->S, p->Hkv, p->B, d.pr.k_st, bk, bf) ||
-      !map16(&m.v, v, p->Dv, p->S, p->Hkv, p->B, d.pr.v_st, bk, bf))
+  if (!map16(&m.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, 128, bf) || !map16(&m.k, k, p->Dqk, d.pr.Sk, p->Hkv, p->B, d.pr.k_st, bk, bf) ||
+      !map16(&m.v, v, p->Dv, d.pr.Sk, p->Hkv, p->B, d.pr.v_st, bk, bf))
     return GQA_ERR_CUDA;
   return to_status(launch_fwd(d.pr, bf, m, sink, o, lse, static_cast<cudaStream_t>(stream)));
 }
@@ -233,8 +246,15 @@ gqa_status gqa_attn_bwd_preprocess(const gqa_attn_params* p, const void* o, cons
   if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(lse, 4) || !aligned(delta, 4)) return GQA_ERR_INVALID_ARG;
   if (p->S == 0) return GQA_OK;
   Derived d = derive(p, workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d.need_dkdv_acc) {  // the dK / dV accumulators span the key axis: zeroed here, not per query row
+    const size_t rows = static_cast<size_t>(p->B) * p->Hkv * d.pr.Sk;
+    if (cudaMemsetAsync(d.pr.dk_acc, 0, rows * p->Dqk * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(d.pr.dv_acc, 0, rows * p->Dv * 4, st) != cudaSuccess)
+      return GQA_ERR_CUDA;
+  }
   return to_status(launch_preprocess(d.pr, p->dtype == GQA_BF16, o, dout, lse, delta, d.need_dq_acc,
-                                     d.need_dkdv_acc, num_sms(), static_cast<cudaStream_t>(stream)));
+                                     num_sms(), st));
 }
 
 gqa_status gqa_attn_bwd(const gqa_attn_params* p, const void* q, const void* k, const void* v, const void* dout,
@@ -254,11 +274,11 @@ gqa_status gqa_attn_bwd(const gqa_attn_params* p, const void* q, const void* k, 
   Maps m;
   std::memset(&m, 0, sizeof(m));
   if (!map16(&m.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, bq, bf) || !map16(&m.dout, dout, p->Dv, p->S, p->Hq, p->B, d.pr.do_st, bq, bf) ||
-      !map16(&m.k, k, p->Dqk, p->S, p->Hkv, p->B, d.pr.k_st, 128, bf) || !map16(&m.v, v, p->Dv, p->S, p->Hkv, p->B, d.pr.v_st, 128, bf))
+      !map16(&m.k, k, p->Dqk, d.pr.Sk, p->Hkv, p->B, d.pr.k_st, 128, bf) || !map16(&m.v, v, p->Dv, d.pr.Sk, p->Hkv, p->B, d.pr.v_st, 128, bf))
     return GQA_ERR_CUDA;
   if (d.need_dq_acc && !map32(&m.dq_acc, d.pr.dq_acc, p->Dqk, p->S, p->B * p->Hq)) return GQA_ERR_CUDA;
-  if (d.need_dkdv_acc && (!map32(&m.dk_acc, d.pr.dk_acc, p->Dqk, p->S, p->B * p->Hkv) ||
-                          !map32(&m.dv_acc, d.pr.dv_acc, p->Dv, p->S, p->B * p->Hkv)))
+  if (d.need_dkdv_acc && (!map32(&m.dk_acc, d.pr.dk_acc, p->Dqk, d.pr.Sk, p->B * p->Hkv) ||
+                          !map32(&m.dv_acc, d.pr.dv_acc, p->Dv, d.pr.Sk, p->B * p->Hkv)))
     return GQA_ERR_CUDA;
   static const int red_to_mode[4] = {kDqRedV4, kDqBulk, kDqScalar, kDqStore};
   KvLaunch kl;
@@ -275,7 +295,7 @@ gqa_status gqa_attn_bwd(const gqa_attn_params* p, const void* q, const void* k, 
     const int bk = q_kernel_bk();
     if (!map16(&m2.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, 128, bf) ||
         !map16(&m2.dout, dout, p->Dv, p->S, p->Hq, p->B, d.pr.do_st, 128, bf) ||
-        !map16(&m2.k, k, p->Dqk, p->S, p->Hkv, p->B, d.pr.k_st, bk, bf) || !map16(&m2.v, v, p->Dv, p->S, p->Hkv, p->B, d.pr.v_st, bk, bf))
+        !map16(&m2.k, k, p->Dqk, d.pr.Sk, p->Hkv, p->B, d.pr.k_st, bk, bf) || !map16(&m2.v, v, p->Dv, d.pr.Sk, p->Hkv, p->B, d.pr.v_st, bk, bf))
       return GQA_ERR_CUDA;
     e = launch_dq(d.pr, bf, m2, dq, st);
     if (e != cudaSuccess) return GQA_ERR_CUDA;
@@ -300,8 +320,8 @@ gqa_status gqa_attn_bwd_postprocess(const gqa_attn_params* p, void* dq, void* dk
     if (e != cudaSuccess) return GQA_ERR_CUDA;
   }
   if (d.need_dkdv_acc) {
-    cudaError_t e = launch_cast(d.pr.dk_acc, dk, p->B, p->Hkv, p->S, p->Dqk, d.pr.dk_st, p->scale, bf, sms, st);
-    if (e == cudaSuccess) e = launch_cast(d.pr.dv_acc, dv, p->B, p->Hkv, p->S, p->Dv, d.pr.dv_st, 1.f, bf, sms, st);
+    cudaError_t e = launch_cast(d.pr.dk_acc, dk, p->B, p->Hkv, d.pr.Sk, p->Dqk, d.pr.dk_st, p->scale, bf, sms, st);
+    if (e == cudaSuccess) e = launch_cast(d.pr.dv_acc, dv, p->B, p->Hkv, d.pr.Sk, p->Dv, d.pr.dv_st, 1.f, bf, sms, st);
     if (e != cudaSuccess) return GQA_ERR_CUDA;
   }
   return GQA_OK;

@@ -50,6 +50,10 @@ struct Problem {
   float* dv_acc;      // [B][Hkv][S][Dv] fp32
   // layouts of the caller's 16-bit tensors (element offset of row (b, h, s) = row(b, h, s))
   Strides q_st, k_st, v_st, o_st, do_st, dq_st, dk_st, dv_st;
+  // keys: rows per batch (or packed key tokens), device key offsets (or null: cu_seqlens), longest
+  int Sk;
+  const int32_t* cu_seqlens_k;
+  int max_len_k;
 };
 
 // One sequence of the (possibly packed) batch.
@@ -83,6 +87,43 @@ __device__ __forceinline__ bool load_seq(const Problem& p, int s, Seq& q) {
   return true;
 }
 
+// The keys of sequence s (same checks as load_seq, against the key axis).
+__device__ __forceinline__ bool load_kseq(const Problem& p, int s, Seq& k) {
+  const int32_t* cu = p.cu_seqlens_k ? p.cu_seqlens_k : p.cu_seqlens;
+  if (cu) {
+    const int a = __ldg(cu + s), e = __ldg(cu + s + 1);
+    k.b = 0;
+    k.start = a;
+    k.len = e - a;
+    if (k.len < 0 || a < 0 || e > p.Sk) {
+      atomicCAS(p.err, 0, kErrBadSeqlens);
+      k.len = 0;
+      return false;
+    }
+    if (k.len > p.max_len_k) {
+      atomicCAS(p.err, 0, kErrSeqTooLong);
+      k.len = 0;
+      return false;
+    }
+  } else {
+    k.b = s;
+    k.start = 0;
+    k.len = p.Sk;
+  }
+  return true;
+}
+
+// Is key j (local) visible to query i (local)?  off = Lk - Lq aligns the causal diagonal at the
+// bottom right (0 when a sequence has as many keys as queries).
+__host__ __device__ __forceinline__ bool visible(int i, int j, int len_k, int off, int causal, int window) {
+  return j < len_k && (!causal || j <= i + off) && (window <= 0 || i + off - j < window);
+}
+// The same test from the pair's diagonal distance d = i + off - j and whether key j exists: the
+// tile loops hoist everything but a compile-time offset into d, two comparisons per element.
+__device__ __forceinline__ bool visible_d(int d, bool key_exists, int causal, int window) {
+  return key_exists && (!causal || d >= 0) && (window <= 0 || d < window);
+}
+
 // Index of the first float of a stats tile: head h, sequence s, 128-row tile t.
 __host__ __device__ __forceinline__ size_t stat_index(const Problem& p, int h, int s, int t) {
   return ((static_cast<size_t>(h) * p.nseqs + s) * p.ntiles + t) * kStatTile;
@@ -97,7 +138,7 @@ constexpr int kFoldRowBytes = 32;  // 16 fp16 values per query row in an xfold t
 
 __host__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Dqk, int Dv, int nseqs, int ntiles,
+__host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Sk, int Dqk, int Dv, int nseqs, int ntiles,
                                    bool need_dq_acc, bool need_dkdv_acc, bool need_fold) {
   WsLayout w{};
   size_t off = 0;
@@ -113,30 +154,35 @@ __host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Dqk, int D
   w.dq_off = off;
   if (need_dq_acc) off = align256(off + static_cast<size_t>(B) * Hq * S * Dqk * 4);
   w.dk_off = off;
-  if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * S * Dqk * 4);
+  if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * Sk * Dqk * 4);
   w.dv_off = off;
-  if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * S * Dv * 4);
+  if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * Sk * Dv * 4);
   w.total = off;
   return w;
 }
 
 // ---------------------------------------------------------------- tile ranges
-// Query rows i (local to the sequence) that can see some key of the 128-row
-// KV tile kt, as a range of query tiles of `bq` rows: [*t0, *t1).
-__host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len, int bq, int causal, int window,
-                                                             int* t0, int* t1) {
-  const int ntq = (len + bq - 1) / bq;
+// (len_q queries and len_k keys in the sequence; off = len_k - len_q; see `visible`)
+
+// Query rows that can see some key of the 128-row KV tile kt, as a range of query tiles of
+// `bq` rows: [*t0, *t1).
+__host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len_q, int len_k, int bq, int causal,
+                                                             int window, int* t0, int* t1) {
+  const int ntq = (len_q + bq - 1) / bq;
   if (!causal) {
     *t0 = 0;
     *t1 = ntq;
     return;
   }
-  const int j_lo = kt * 128;
-  int a = j_lo / bq;
+  const long long off = static_cast<long long>(len_k) - len_q;
+  const long long j_lo = static_cast<long long>(kt) * 128;
+  const long long i_first = j_lo - off;  // first row whose diagonal reaches the tile
+  int a = i_first > 0 ? static_cast<int>(i_first / bq) : 0;
+  if (a > ntq) a = ntq;
   int b = ntq;
   if (window > 0) {
-    const long long i_hi = static_cast<long long>(j_lo) + 127 + window - 1;  // last row seeing key j_lo+127
-    const long long tb = i_hi / bq + 1;
+    const long long i_hi = j_lo + 127 + window - 1 - off;  // last row seeing key j_lo + 127
+    const long long tb = i_hi < 0 ? 0 : i_hi / bq + 1;
     if (tb < b) b = static_cast<int>(tb);
   }
   *t0 = a;
@@ -144,21 +190,22 @@ __host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len, in
 }
 
 // Key tiles of `bk` rows visible to the query tile qt of 128 rows: [*k0, *k1).
-__host__ __device__ __forceinline__ void kv_tiles_for_q_tile(int qt, int len, int bk, int causal, int window, int* k0,
-                                                             int* k1) {
-  const int ntk = (len + bk - 1) / bk;
+__host__ __device__ __forceinline__ void kv_tiles_for_q_tile(int qt, int len_q, int len_k, int bk, int causal,
+                                                             int window, int* k0, int* k1) {
+  const int ntk = (len_k + bk - 1) / bk;
   if (!causal) {
     *k0 = 0;
     *k1 = ntk;
     return;
   }
-  const int i_lo = qt * 128, i_hi = qt * 128 + 127;
-  int b = i_hi / bk + 1;
+  const long long off = static_cast<long long>(len_k) - len_q;
+  const long long d_lo = static_cast<long long>(qt) * 128 + off, d_hi = d_lo + 127;  // diagonals of the tile
+  int b = d_hi < 0 ? 0 : static_cast<int>(d_hi / bk + 1);
   if (b > ntk) b = ntk;
   int a = 0;
   if (window > 0) {
-    const int j_lo = i_lo - window + 1;
-    a = j_lo > 0 ? j_lo / bk : 0;
+    const long long j_lo = d_lo - window + 1;
+    a = j_lo > 0 ? static_cast<int>(j_lo / bk) : 0;
   }
   *k0 = a;
   *k1 = b > a ? b : a;

@@ -61,7 +61,7 @@ __device__ __forceinline__ void write_fold_row(uint8_t* tile, int q, float xl, f
 template <typename T, int DV>
 __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __restrict__ o,
                                                          const T* __restrict__ dout, const float* __restrict__ lse,
-                                                         float* __restrict__ delta, int zero_dq, int zero_dkdv) {
+                                                         float* __restrict__ delta, int zero_dq) {
   constexpr int PER = DV / 8;        // elements per thread
   constexpr int VEC = PER / 8;       // uint4 loads per thread per tensor
   const long long nrows = static_cast<long long>(p.B) * p.Hq * p.S;
@@ -126,13 +126,6 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
     if (zero_dq) {
       float4* z = reinterpret_cast<float4*>(p.dq_acc + r * p.Dqk);
       for (int c = sub; c < p.Dqk / 4; c += 8) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (zero_dkdv && h < p.Hkv) {
-      const long long rk = (static_cast<long long>(b) * p.Hkv + h) * p.S + i;
-      float4* zk = reinterpret_cast<float4*>(p.dk_acc + rk * p.Dqk);
-      for (int c = sub; c < p.Dqk / 4; c += 8) zk[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      float4* zv = reinterpret_cast<float4*>(p.dv_acc + rk * p.Dv);
-      for (int c = sub; c < p.Dv / 4; c += 8) zv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
@@ -203,7 +196,7 @@ __global__ void selftest_wait_kernel(int* err, long long limit) {
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_preprocess(const Problem& p, int dtype_bf16, const void* o, const void* dout, const float* lse,
-                              float* delta, bool zero_dq, bool zero_dkdv, int num_sms, cudaStream_t st) {
+                              float* delta, bool zero_dq, int num_sms, cudaStream_t st) {
   const long long rows = static_cast<long long>(p.B) * p.Hq * p.S;
   long long blocks = (rows + 31) / 32;
   const long long cap = static_cast<long long>(num_sms) * 8;
@@ -211,7 +204,7 @@ cudaError_t launch_preprocess(const Problem& p, int dtype_bf16, const void* o, c
   if (blocks < 1) blocks = 1;
 #define GQA_PRE(T, DV)                                                                                \
   preprocess_kernel<T, DV><<<static_cast<unsigned>(blocks), 256, 0, st>>>(                            \
-      p, static_cast<const T*>(o), static_cast<const T*>(dout), lse, delta, zero_dq, zero_dkdv)
+      p, static_cast<const T*>(o), static_cast<const T*>(dout), lse, delta, zero_dq)
   if (dtype_bf16) {
     if (p.Dv == 64) GQA_PRE(__nv_bfloat16, 64);
     else GQA_PRE(__nv_bfloat16, 128);

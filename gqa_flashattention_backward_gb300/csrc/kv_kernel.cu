@@ -99,9 +99,6 @@ struct KvCtl {
 };
 static_assert(sizeof(KvCtl) <= 256, "ctl");
 
-__device__ __forceinline__ bool kv_allowed(int i, int j, int len, int causal, int window) {
-  return j < len && (!causal || j <= i) && (window <= 0 || i - j < window);
-}
 
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
   asm volatile(
@@ -187,9 +184,10 @@ __global__ void __launch_bounds__(448, 1)
 
   const int head = blockIdx.x;   // kv head (group_tmem) or query head
   const int s = blockIdx.z;
-  Seq sq;
-  if (!load_seq(p, s, sq)) return;
-  const int ntk = (sq.len + C::BK - 1) / C::BK;
+  Seq sq, sk;  // the sequence's queries and keys
+  if (!load_seq(p, s, sq) || !load_kseq(p, s, sk)) return;
+  const int off = sk.len - sq.len;  // query i sits on key diagonal i + off
+  const int ntk = (sk.len + C::BK - 1) / C::BK;
   const int kt = blockIdx.y;     // tile 0 has the most query tiles under a causal mask: launched first
   if (kt >= ntk) return;
   if ((smem_u32(smem) & 1023u) != 0) {  // the operand layout needs a 1024-byte aligned base
@@ -197,7 +195,7 @@ __global__ void __launch_bounds__(448, 1)
     return;
   }
   int t0, t1;
-  q_tiles_for_kv_tile(kt, sq.len, C::BQ, p.causal, p.window, &t0, &t1);
+  q_tiles_for_kv_tile(kt, sq.len, sk.len, C::BQ, p.causal, p.window, &t0, &t1);
   const int nt = t1 - t0;
   const int g = group_tmem ? head : head / p.G;
   const int nh = group_tmem ? p.G : 1;
@@ -254,11 +252,11 @@ __global__ void __launch_bounds__(448, 1)
       tma_prefetch_map(&m.q);
       tma_prefetch_map(&m.dout);
       mbar_expect_tx(&ctl.kv_full, C::K_BYTES + C::V_BYTES);
-      const int krow = sq.start + j0;
+      const int krow = sk.start + j0;
       for (int cb = 0; cb < DQK / 64; ++cb)
-        tma_load_4d(smem + C::OFF_K + cb * (C::BK * 128), &m.k, &ctl.kv_full, cb * 64, krow, g, sq.b);
+        tma_load_4d(smem + C::OFF_K + cb * (C::BK * 128), &m.k, &ctl.kv_full, cb * 64, krow, g, sk.b);
       for (int cb = 0; cb < DV / 64; ++cb)
-        tma_load_4d(smem + C::OFF_V + cb * (C::BK * 128), &m.v, &ctl.kv_full, cb * 64, krow, g, sq.b);
+        tma_load_4d(smem + C::OFF_V + cb * (C::BK * 128), &m.v, &ctl.kv_full, cb * 64, krow, g, sk.b);
       int issued = 0;
       for (int it = 0; it < NIT; ++it) {
         const int st = it % C::ST;
@@ -509,8 +507,8 @@ __global__ void __launch_bounds__(448, 1)
       const int st = it % C::ST;
       const int t = t0 + it % nt;
       const int i0 = t * C::BQ;
-      const bool need_mask = (j0 + C::BK > sq.len) || (p.causal && i0 < j0 + C::BK - 1) ||
-                             (p.window > 0 && i0 + C::BQ - 1 - j0 >= p.window);
+      const bool need_mask = (j0 + C::BK > sk.len) || (p.causal && i0 + off < j0 + C::BK - 1) ||
+                             (p.window > 0 && i0 + C::BQ - 1 + off - j0 >= p.window);
       const float4* sL4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE) + (st * C::BQ + cbase) / 4;
       const float4* sD4 = reinterpret_cast<const float4*>(smem + C::OFF_DEL) + (st * C::BQ + cbase) / 4;
       // exponent arguments of four consecutive columns: S*scale*log2e - LSE2 (with the fold the MMA
@@ -565,10 +563,10 @@ __global__ void __launch_bounds__(448, 1)
           }
         }
         if (need_mask) {
+          const int d0 = i0 + cbase + 32 * c + off - j;  // diagonal distance of this chunk's first query
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (!kv_allowed(i0 + cbase + 32 * c + e, j, sq.len, p.causal, p.window))
-              pk[16 * c + e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+            if (!visible_d(d0 + e, j < sk.len, p.causal, p.window)) pk[16 * c + e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
         }
         uint32_t pc[16];
 #pragma unroll
@@ -631,8 +629,8 @@ __global__ void __launch_bounds__(448, 1)
     // warpgroup 0 writes dV, warpgroup 1 writes dK (both cover all 128 key rows)
     if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 24)) {
       tc_fence_after();
-      const bool valid = j < sq.len;
-      const size_t krow = static_cast<size_t>(zk) * p.S + sq.start + j;
+      const bool valid = j < sk.len;
+      const size_t krow = static_cast<size_t>(zk) * p.Sk + sk.start + j;
       uint8_t* stg = smem + C::OFF_Q + warp * (2 * 32 * 32 * 4);  // stage buffers are idle now
       int nbulk = 0;
       auto emit = [&](uint32_t tcol, int D, void* out, const Strides& ost, float* acc, const CUtensorMap* map,
@@ -645,7 +643,7 @@ __global__ void __launch_bounds__(448, 1)
             for (int e = 0; e < 32; ++e) v[e] = 0u;
           if (group_tmem) {
             if (valid) {
-              T* o = static_cast<T*>(out) + ost.row(sq.b, g, sq.start + j) + c0;
+              T* o = static_cast<T*>(out) + ost.row(sk.b, g, sk.start + j) + c0;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 uint4 w;
@@ -666,7 +664,7 @@ __global__ void __launch_bounds__(448, 1)
             uint8_t* buf = stg + (nbulk & 1) * (32 * 32 * 4);
             if (lane == 0 && nbulk >= 1) bulk_wait_read1();
             __syncwarp();
-            stage_and_reduce(buf, map, lane, v, c0, sq.start + j0 + (warp & 3) * 32, zk);
+            stage_and_reduce(buf, map, lane, v, c0, sk.start + j0 + (warp & 3) * 32, zk);
             ++nbulk;
           }
         }
@@ -692,7 +690,7 @@ static cudaError_t launch_kv_t(const Problem& p, const Maps& m, const KvLaunch& 
   auto kern = kv_kernel<DQK, DV, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int ntk = (p.max_len + C::BK - 1) / C::BK;
+  const int ntk = (p.max_len_k + C::BK - 1) / C::BK;
   if (ntk == 0 || p.nseqs == 0) return cudaSuccess;
   dim3 grid(kl.group_tmem ? p.Hkv : p.Hq, ntk, p.nseqs);
   kern<<<grid, C::THREADS, C::SMEM, st>>>(p, m, kl.group_tmem, C::HAS_DQ ? kl.dq_mode : kDqNone, kl.kv_red_mode,

@@ -25,7 +25,7 @@ struct KvLaunch {
 };
 
 cudaError_t launch_preprocess(const Problem& p, int dtype_bf16, const void* o, const void* dout, const float* lse,
-                              float* delta, bool zero_dq, bool zero_dkdv, int num_sms, cudaStream_t st);
+                              float* delta, bool zero_dq, int num_sms, cudaStream_t st);
 cudaError_t launch_cast(const float* acc, void* out, int B, int H, int S, int D, const Strides& st, float mul,
                         int dtype_bf16, int num_sms, cudaStream_t st_);
 cudaError_t launch_dsink(int B, int Hq, int S, const float* sink, const float* lse, const float* delta,

@@ -73,10 +73,6 @@ struct QSmemCtl {
   float stat_m[2][128];  // FWD: each warpgroup's row maxima, combined once
 };
 
-// Allowed-key test for query row i (local) and key j (local).
-__device__ __forceinline__ bool allowed(int i, int j, int len, int causal, int window) {
-  return j < len && (!causal || j <= i) && (window <= 0 || i - j < window);
-}
 
 template <int DQK, int DV, bool BF16, bool FWD>
 __global__ void __launch_bounds__(320, 1)
@@ -93,13 +89,14 @@ __global__ void __launch_bounds__(320, 1)
 
   const int h = blockIdx.x;
   const int s = blockIdx.z;
-  Seq sq;
-  if (!load_seq(p, s, sq)) return;
+  Seq sq, sk;  // the sequence's queries and keys
+  if (!load_seq(p, s, sq) || !load_kseq(p, s, sk)) return;
+  const int off = sk.len - sq.len;  // query i sits on key diagonal i + off
   const int ntq = (sq.len + C::BQ - 1) / C::BQ;
   const int t = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tiles first
   if (t >= ntq) return;
   int k0, k1;
-  kv_tiles_for_q_tile(t, sq.len, C::BK, p.causal, p.window, &k0, &k1);
+  kv_tiles_for_q_tile(t, sq.len, sk.len, C::BK, p.causal, p.window, &k0, &k1);
   const int n = k1 - k0;
   const int NIT = FWD ? 2 * n : n;
   const int g = h / p.G;
@@ -163,12 +160,12 @@ __global__ void __launch_bounds__(320, 1)
         uint8_t* sK = sK0 + st * C::STAGE_BYTES;
         uint8_t* sV = sK + C::K_BYTES;
         mbar_expect_tx(&ctl.kv_full[st], C::K_BYTES + (need_v ? C::V_BYTES : 0));
-        const int krow = sq.start + kt * C::BK;
+        const int krow = sk.start + kt * C::BK;
         for (int cb = 0; cb < C::QB; ++cb)
-          tma_load_4d(sK + cb * (C::BK * 128), &m.k, &ctl.kv_full[st], cb * 64, krow, g, sq.b);
+          tma_load_4d(sK + cb * (C::BK * 128), &m.k, &ctl.kv_full[st], cb * 64, krow, g, sk.b);
         if (need_v)
           for (int cb = 0; cb < C::VB; ++cb)
-            tma_load_4d(sV + cb * (C::BK * 128), &m.v, &ctl.kv_full[st], cb * 64, krow, g, sq.b);
+            tma_load_4d(sV + cb * (C::BK * 128), &m.v, &ctl.kv_full[st], cb * 64, krow, g, sk.b);
         issued = it + 1;
       }
       if (ctl.abort_flag) {
@@ -273,8 +270,8 @@ __global__ void __launch_bounds__(320, 1)
       for (int it = w, k = 0; it < NIT; it += 2, ++k) {
         const int kt = k0 + it % n;
         const int j0 = kt * C::BK;
-        const bool need_mask = (j0 + C::BK > sq.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ) ||
-                               (p.window > 0 && t * C::BQ + C::BQ - 1 - j0 >= p.window);
+        const bool need_mask = (j0 + C::BK > sk.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ + off) ||
+                               (p.window > 0 && t * C::BQ + C::BQ - 1 + off - j0 >= p.window);
         if (it >= n && !combined) combine();
         if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
           ok = false;
@@ -290,8 +287,9 @@ __global__ void __launch_bounds__(320, 1)
           for (int e = 0; e < C::BK; e += 2) {
             float a = __uint_as_float(v[e]), b = __uint_as_float(v[e + 1]);
             if (need_mask) {
-              if (!allowed(il, j0 + e, sq.len, p.causal, p.window)) a = -INFINITY;
-              if (!allowed(il, j0 + e + 1, sq.len, p.causal, p.window)) b = -INFINITY;
+              const int d0 = il + off - j0;  // diagonal distance to this tile's first key
+              if (!visible_d(d0 - e, j0 + e < sk.len, p.causal, p.window)) a = -INFINITY;
+              if (!visible_d(d0 - e - 1, j0 + e + 1 < sk.len, p.causal, p.window)) b = -INFINITY;
             }
             c0 = fmaxf(c0, a);
             c1 = fmaxf(c1, b);
@@ -318,7 +316,8 @@ __global__ void __launch_bounds__(320, 1)
           if (need_mask) {
 #pragma unroll
             for (int e = 0; e < C::BK; ++e)
-              if (!allowed(il, j0 + e, sq.len, p.causal, p.window)) pk[e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+              if (!visible_d(il + off - j0 - e, j0 + e < sk.len, p.causal, p.window))
+                pk[e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
           }
           uint32_t p0[16], p1[16];
 #pragma unroll
@@ -377,8 +376,8 @@ __global__ void __launch_bounds__(320, 1)
       for (int it = w, k = 0; it < NIT; it += 2, ++k) {
         const int kt = k0 + it;
         const int j0 = kt * C::BK;
-        const bool need_mask = (j0 + C::BK > sq.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ) ||
-                               (p.window > 0 && t * C::BQ + C::BQ - 1 - j0 >= p.window);
+        const bool need_mask = (j0 + C::BK > sk.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ + off) ||
+                               (p.window > 0 && t * C::BQ + C::BQ - 1 + off - j0 >= p.window);
         if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
           ok = false;
           break;
@@ -395,8 +394,9 @@ __global__ void __launch_bounds__(320, 1)
             float pa = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, nlse2));
             float pb = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, nlse2));
             if (need_mask) {
-              if (!allowed(il, j0 + c0 + 2 * e, sq.len, p.causal, p.window)) pa = 0.f;
-              if (!allowed(il, j0 + c0 + 2 * e + 1, sq.len, p.causal, p.window)) pb = 0.f;
+              const int d0 = il + off - j0 - c0;  // diagonal distance to this chunk's first key
+              if (!visible_d(d0 - 2 * e, j0 + c0 + 2 * e < sk.len, p.causal, p.window)) pa = 0.f;
+              if (!visible_d(d0 - 2 * e - 1, j0 + c0 + 2 * e + 1 < sk.len, p.causal, p.window)) pb = 0.f;
             }
             const float da = pa * (__uint_as_float(dv[2 * e]) + ndlt);
             const float db = pb * (__uint_as_float(dv[2 * e + 1]) + ndlt);

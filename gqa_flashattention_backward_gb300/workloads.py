@@ -49,6 +49,27 @@ class Workload:
     varlen_lengths: Optional[List[int]] = None
     scale: Optional[float] = None
     extra: dict = field(default_factory=dict)
+    Sk: Optional[int] = None                      # key rows (or packed key tokens); None: S
+    varlen_lengths_k: Optional[List[int]] = None  # per-sequence key counts; None: varlen_lengths
+
+    @property
+    def key_len(self) -> int:
+        return self.Sk if self.Sk is not None else self.S
+
+    @property
+    def cu_seqlens_k(self) -> Optional[List[int]]:
+        if self.varlen_lengths_k is None:
+            return None
+        cu = [0]
+        for n in self.varlen_lengths_k:
+            cu.append(cu[-1] + n)
+        return cu
+
+    @property
+    def max_seqlen_k(self) -> int:
+        if self.varlen_lengths_k:
+            return max(self.varlen_lengths_k)
+        return self.max_seqlen if self.varlen_lengths else self.key_len
 
     @property
     def resolved_scale(self) -> float:
@@ -150,8 +171,8 @@ def make_inputs(w: Workload, seed: Optional[int] = None):
         return t.to(w.dtype)
 
     q = draw((w.B, w.Hq, w.S, w.Dqk), w.qkv_std)
-    k = draw((w.B, w.Hkv, w.S, w.Dqk), w.qkv_std)
-    v = draw((w.B, w.Hkv, w.S, w.Dv), w.qkv_std)
+    k = draw((w.B, w.Hkv, w.key_len, w.Dqk), w.qkv_std)
+    v = draw((w.B, w.Hkv, w.key_len, w.Dv), w.qkv_std)
     dout = draw((w.B, w.Hq, w.S, w.Dv), 1.0)
     sink = torch.randn((w.Hq,), generator=g, dtype=torch.float32) if w.sink else None
     return q, k, v, dout, sink

@@ -92,11 +92,15 @@ typedef struct {
 
 typedef struct {
   int B, Hq, Hkv;        /* batch, query heads, kv heads; Hq % Hkv == 0 (group size Hq/Hkv) */
-  int S;                 /* sequence length, or total packed tokens T when cu_seqlens != NULL */
+  int S;                 /* query rows per batch, or total packed query tokens when cu_seqlens != NULL;
+                            also the key rows unless Sk (below) says otherwise */
   int Dqk, Dv;           /* head dims: (64,64), (128,128) or (192,128) */
   gqa_dtype dtype;
-  int causal;            /* 1: key j visible to query i iff j <= i (top-left; Sq == Sk) */
-  int window;            /* > 0: also require i - j < window (requires causal); <= 0: none */
+  int causal;            /* 1: key j visible to query i iff j <= i + (Lk - Lq) for a sequence of Lq
+                            queries and Lk keys: the diagonal aligned at the bottom right, i.e.
+                            j <= i when Lq == Lk (query rows that see no key get O = 0, LSE = -inf
+                            or the sink alone, and zero gradients) */
+  int window;            /* > 0: also require i + (Lk - Lq) - j < window (requires causal); <= 0: none */
   float scale;           /* softmax scale on Q.K^T, finite and > 0; typically 1/sqrt(Dqk) */
   const int32_t* cu_seqlens; /* DEVICE int32 [nseq+1], cu[0] = 0, non-decreasing, cu[nseq] = S;
                                 NULL for dense batches.  Requires B == 1. */
@@ -112,6 +116,14 @@ typedef struct {
    * inputs q, k, v, o (read by the backward preprocess, written by the forward), dout; outputs
    * dq, dk, dv.  LSE, Delta and dsink stay contiguous fp32 [B, Hq, S] / [Hq]. */
   gqa_stride q_st, k_st, v_st, o_st, do_st, dq_st, dk_st, dv_st;
+  /* Keys fewer or more than queries (chunked prefill, a KV cache, cross-attention); all zero /
+   * NULL: the same as the queries. */
+  int Sk;                /* key rows per batch (k, v, dk, dv are [B,Hkv,Sk,D]), or total packed key
+                            tokens; 0: Sk = S */
+  const int32_t* cu_seqlens_k; /* DEVICE int32 [nseq+1] key offsets of the packed sequences (same
+                                  rules as cu_seqlens, cu[nseq] = Sk), or NULL: the same offsets
+                                  as cu_seqlens; requires cu_seqlens */
+  int max_seqlen_k;      /* upper bound on every packed key length; 0: max_seqlen */
 } gqa_attn_params;
 
 /* Bytes of workspace every call below needs for `p` (0 if `p` is invalid).  The
