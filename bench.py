@@ -44,6 +44,40 @@ def _dist():
     return ws, rank, local
 
 
+class Ranks:
+    """The replicas' coordination under torchrun (one process per GPU, nothing shared in the data
+    path): barrier, the maximum of a time over ranks, teardown.  `backend` is "nccl" on the GPUs
+    and "gloo" in the CPU tests of this logic."""
+
+    def __init__(self, backend: str, device):
+        import torch.distributed as dist
+        self.dist = dist
+        self.ws, self.rank, self.local = _dist()
+        self.device = device
+        if self.ws > 1 and not dist.is_initialized():
+            if backend == "nccl":
+                dist.init_process_group(backend, device_id=device)
+            else:
+                dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.ws > 1:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.ws == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.ws > 1:
+            self.dist.barrier()
+            self.dist.destroy_process_group()
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -135,7 +169,6 @@ def _traffic(kernel_key: str, src_hash: str):
 
 def run_gpu(args):
     import torch
-    import torch.distributed as dist
 
     import gqa_flashattention_backward_gb300 as pkg
     from gqa_flashattention_backward_gb300 import _native as nat
@@ -144,12 +177,8 @@ def run_gpu(args):
     ws_n, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if ws_n > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if ws_n > 1:
-            dist.barrier()
+    ranks = Ranks("nccl", dev)
+    barrier = ranks.barrier
 
     nat.load()
     peaks = _peaks()
@@ -207,12 +236,7 @@ def run_gpu(args):
         main_ms = sum(a.elapsed_time(b) for a, b in evs) / steps if main_events else None
         return ms, main_ms, launches
 
-    def max_over_ranks(x):
-        if ws_n == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = ranks.max
 
     w = W.mha_causal(args.n_ctx)
     c = setup(w)
@@ -406,9 +430,7 @@ def run_gpu(args):
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clocks,
                     variants=variants, sweep=sweep, configs=configs, forward=forward)
         print(json.dumps(line), flush=True)
-    if ws_n > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+    ranks.close()
     return line
 
 
