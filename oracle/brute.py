@@ -15,9 +15,10 @@ import numpy as np
 
 
 def mask_matrix(S: int, causal: bool, window: int, cu_seqlens: Optional[Sequence[int]], Sk: Optional[int] = None,
-                cu_seqlens_k: Optional[Sequence[int]] = None) -> np.ndarray:
+                cu_seqlens_k: Optional[Sequence[int]] = None, window_right: int = 0) -> np.ndarray:
     """allowed[i, j] for query row i and key row j: same sequence, and with local indices
-    il, jl and the sequence's lengths Lq, Lk, causal jl <= il + Lk - Lq, window il + Lk - Lq - jl < W."""
+    il, jl and the sequence's lengths Lq, Lk, causal jl <= il + Lk - Lq, window il + Lk - Lq - jl < W,
+    right window jl - (il + Lk - Lq) < Wr."""
     Sk = Sk or S
     cu_q = list(cu_seqlens) if cu_seqlens is not None else [0, S]
     cu_k = list(cu_seqlens_k) if cu_seqlens_k is not None else (list(cu_seqlens) if cu_seqlens is not None
@@ -38,6 +39,8 @@ def mask_matrix(S: int, causal: bool, window: int, cu_seqlens: Optional[Sequence
         allowed &= jl <= diag
     if window > 0:
         allowed &= (diag - jl) < window
+    if window_right > 0 and not causal:
+        allowed &= (jl - diag) < window_right
     return allowed
 
 
@@ -70,13 +73,13 @@ def mha_head(q, k, v, dout, scale, allowed, sink: Optional[float]):
     return dict(O=O, LSE=lse, P=P, p_sink=p_sink, dP=dP, dS=dS, Delta=Delta, dQ=dQ, dK=dK, dV=dV, dsink=dsink)
 
 
-def gqa(q, k, v, dout, scale, causal=True, window=0, cu_seqlens=None, sink=None, cu_seqlens_k=None):
+def gqa(q, k, v, dout, scale, causal=True, window=0, cu_seqlens=None, sink=None, cu_seqlens_k=None, window_right=0):
     """Full GQA forward+backward for [B,H,S,D] float64 arrays via per-head MHA (k, v may have
     another length Sk)."""
     B, Hq, S, _ = q.shape
     Hkv, Sk = k.shape[1], k.shape[2]
     G = Hq // Hkv
-    allowed = mask_matrix(S, causal, window, cu_seqlens, Sk, cu_seqlens_k)
+    allowed = mask_matrix(S, causal, window, cu_seqlens, Sk, cu_seqlens_k, window_right)
     out = dict(
         o=np.zeros((B, Hq, S, v.shape[3])), lse=np.zeros((B, Hq, S)), delta=np.zeros((B, Hq, S)),
         dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v), dsink=np.zeros(Hq),

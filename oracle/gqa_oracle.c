@@ -10,7 +10,8 @@
  *   g          = h / (Hq / Hkv)                        ("bx // groups", tilelang
  *                                                       PR #1093, Additional comments)
  *   A(i)       = { j in the same sequence as i, j <= i + (Lk - Lq) if causal,
- *                  i + (Lk - Lq) - j < W if a window W > 0 is set }
+ *                  i + (Lk - Lq) - j < W if a window W > 0 is set,
+ *                  j - (i + (Lk - Lq)) < Wr if a right window Wr > 0 is set (not causal) }
  *                with i, j local to their sequence, Lq / Lk its query / key lengths:
  *                the causal diagonal is aligned at the bottom right (the last query sees
  *                the last key), which is the top-left j <= i when Lq == Lk
@@ -57,6 +58,7 @@ typedef struct {
   const double* sink;  /* [Hq] or NULL */
   int Sk;              /* key rows per batch (or packed key tokens); 0: the same as S */
   const int32_t* cu_seqlens_k; /* [nseq+1] key offsets, or NULL: the same as cu_seqlens */
+  int window_right;    /* > 0 (not causal): keys at most window_right - 1 right of the diagonal */
 } oracle_problem;
 
 static inline int key_len(const oracle_problem* p) { return p->Sk > 0 ? p->Sk : p->S; }
@@ -80,6 +82,7 @@ static void key_range(const oracle_problem* p, int i, int* lo, int* hi) {
   const int il = i - qs, off = kl - ql;  /* query il sits on key diagonal il + off */
   int a = 0, b = kl;
   if (p->causal && il + off + 1 < b) b = il + off + 1;
+  if (!p->causal && p->window_right > 0 && il + off + p->window_right < b) b = il + off + p->window_right;
   if (p->window > 0 && il + off - p->window + 1 > a) a = il + off - p->window + 1;
   *lo = ks + a;
   *hi = ks + b;  /* empty when b <= a */

@@ -40,7 +40,7 @@ class _Problem(ctypes.Structure):
         ("Dqk", ctypes.c_int), ("Dv", ctypes.c_int), ("causal", ctypes.c_int), ("window", ctypes.c_int),
         ("scale", ctypes.c_double), ("nseq", ctypes.c_int),
         ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)), ("sink", ctypes.POINTER(ctypes.c_double)),
-        ("Sk", ctypes.c_int), ("cu_seqlens_k", ctypes.POINTER(ctypes.c_int32)),
+        ("Sk", ctypes.c_int), ("cu_seqlens_k", ctypes.POINTER(ctypes.c_int32)), ("window_right", ctypes.c_int),
     ]
 
 
@@ -80,6 +80,7 @@ class Problem:
     cu_seqlens: Optional[Sequence[int]] = None
     Sk: Optional[int] = None
     cu_seqlens_k: Optional[Sequence[int]] = None
+    window_right: int = 0   # > 0 (not causal): keys j with j - (i + Lk - Lq) < window_right
 
     def resolved_scale(self) -> float:
         return float(self.scale) if self.scale is not None else 1.0 / np.sqrt(self.Dqk)
@@ -120,6 +121,7 @@ def _mk(pb: Problem, sink: Optional[np.ndarray], keep: list):
     else:
         st.sink = ctypes.POINTER(ctypes.c_double)()
     st.Sk = pb.key_len
+    st.window_right = int(pb.window_right)
     if pb.cu_seqlens_k is not None:
         ck = np.ascontiguousarray(np.asarray(pb.cu_seqlens_k, dtype=np.int32))
         keep.append(ck)

@@ -366,3 +366,94 @@ def test_rows_without_keys():
     g2 = orc.backward(pb, q, k, v, o, lse, do2)
     np.testing.assert_array_equal(g["dk"], g2["dk"])
     np.testing.assert_array_equal(g["dv"], g2["dv"])
+
+
+# ---------------------------------------------------------------- right window (local attention)
+# not causal, keys j with j - (i + Lk - Lq) < Wr (and, with a window W, i + Lk - Lq - j < W)
+
+def _local_cases():
+    return [
+        dict(S=9, Sk=9, window=3, wr=2, sink=False, cu=None, cuk=None),    # two-sided, radius 2 / 1
+        dict(S=9, Sk=9, window=0, wr=3, sink=True, cu=None, cuk=None),     # right side only
+        dict(S=6, Sk=10, window=4, wr=4, sink=False, cu=None, cuk=None),   # with Sk != Sq
+        dict(S=7, Sk=7, window=2, wr=3, sink=True, cu=[0, 3, 7], cuk=[0, 4, 7]),
+    ]
+
+
+def _local_pb(c, **shape):
+    shp = dict(TINY, S=c["S"])
+    shp.update(shape)
+    return orc.Problem(causal=False, window=c["window"], window_right=c["wr"], scale=0.7, cu_seqlens=c["cu"],
+                       Sk=c["Sk"], cu_seqlens_k=c["cuk"], **shp)
+
+
+def _local_id(c):
+    return f"q{c['S']}k{c['Sk']}w{c['window']}r{c['wr']}s{int(c['sink'])}{'v' if c['cu'] else ''}"
+
+
+@pytest.mark.parametrize("case", _local_cases(), ids=_local_id)
+def test_right_window_finite_differences(case):
+    pb = _local_pb(case)
+    q, k, v, do, sink = _inputs(pb, seed=29, with_sink=case["sink"])
+    o, lse = orc.forward(pb, q, k, v, sink)
+    g = orc.backward(pb, q, k, v, o, lse, do, sink)
+    h = 1e-5
+
+    def fd(x):
+        num = np.zeros_like(x)
+        flat, nflat = x.reshape(-1), num.reshape(-1)
+        for t in range(flat.size):
+            keep = flat[t]
+            flat[t] = keep + h
+            lp = _loss(pb, q, k, v, do, sink)
+            flat[t] = keep - h
+            lm = _loss(pb, q, k, v, do, sink)
+            flat[t] = keep
+            nflat[t] = (lp - lm) / (2 * h)
+        return num
+
+    for name, x in (("dq", q), ("dk", k), ("dv", v)):
+        num = fd(x)
+        assert np.abs(num - g[name]).max() <= 1e-7 * max(1.0, np.abs(num).max()), name
+
+
+@pytest.mark.parametrize("case", _local_cases(), ids=_local_id)
+def test_right_window_against_bruteforce_and_torch(case):
+    pb = _local_pb(case, Hq=6, Hkv=3, Dqk=6, Dv=4)
+    q, k, v, do, sink = _inputs(pb, seed=31, with_sink=case["sink"])
+    o, lse = orc.forward(pb, q, k, v, sink)
+    g = orc.backward(pb, q, k, v, o, lse, do, sink)
+    r = brute.gqa(q, k, v, do, pb.resolved_scale(), causal=False, window=pb.window, cu_seqlens=pb.cu_seqlens,
+                  sink=sink, cu_seqlens_k=pb.cu_seqlens_k, window_right=pb.window_right)
+    np.testing.assert_allclose(o, r["o"], rtol=0, atol=1e-12)
+    for name in ("dq", "dk", "dv"):
+        np.testing.assert_allclose(g[name], r[name], rtol=0, atol=1e-12, err_msg=name)
+    # PyTorch autograd of softmax attention over the same explicit mask (a library routine)
+    G = pb.Hq // pb.Hkv
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    allowed = torch.tensor(brute.mask_matrix(pb.S, False, pb.window, pb.cu_seqlens, pb.key_len, pb.cu_seqlens_k,
+                                             pb.window_right))
+    logits = torch.einsum("bhid,bhjd->bhij", tq, tk.repeat_interleave(G, dim=1)) * pb.resolved_scale()
+    logits = logits.masked_fill(~allowed, float("-inf"))
+    if sink is not None:
+        logits = torch.cat([logits, torch.tensor(sink).view(1, pb.Hq, 1, 1).expand(pb.B, pb.Hq, pb.S, 1)], dim=-1)
+    probs = torch.nan_to_num(torch.softmax(logits, dim=-1))[..., :pb.key_len]
+    (probs @ tv.repeat_interleave(G, dim=1) * torch.tensor(do)).sum().backward()
+    for name, t in (("dq", tq), ("dk", tk), ("dv", tv)):
+        np.testing.assert_allclose(g[name], t.grad.numpy(), rtol=0, atol=1e-11, err_msg=name)
+
+
+def test_right_window_closed_forms():
+    """A right window of 1 with no left window is the causal mask; left and right windows wider
+    than the sequence are plain non-causal attention."""
+    base = dict(B=1, Hq=4, Hkv=2, S=8, Dqk=5, Dv=3, scale=0.7)
+    a = orc.Problem(causal=False, window_right=1, **base)
+    c = orc.Problem(causal=True, **base)
+    q, k, v, do, _ = _inputs(a, seed=37)
+    oa, la = orc.forward(a, q, k, v)
+    oc, lc = orc.forward(c, q, k, v)
+    np.testing.assert_array_equal(oa, oc)
+    np.testing.assert_array_equal(la, lc)
+    w = orc.Problem(causal=False, window=100, window_right=100, **base)
+    n = orc.Problem(causal=False, **base)
+    np.testing.assert_array_equal(orc.forward(w, q, k, v)[0], orc.forward(n, q, k, v)[0])
