@@ -40,7 +40,7 @@ def preferred_red_mode(Dqk: int) -> int:
 
 
 def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=GQA_GROUP_TMEM,
-            red_mode=None, deterministic=False, cu_seqlens_k=None, max_seqlen_k=None, **tensors):
+            red_mode=None, deterministic=False, cu_seqlens_k=None, max_seqlen_k=None, window_right=0, **tensors):
     """`tensors`: any of o, do, dq, dk, dv whose layouts the call uses.  k / v may have another
     length than q (k.shape[2]): the causal diagonal is then aligned at the bottom right."""
     B, Hq, S, Dqk = q.shape
@@ -55,7 +55,7 @@ def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=G
     return native.make_params(B, Hq, Hkv, S, Dqk, Dv, q.dtype, causal=causal, window=window, scale=scale,
                               cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, group_mode=group_mode,
                               red_mode=red_mode, deterministic=deterministic, strides=strides, Sk=k.shape[2],
-                              cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k)
+                              cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, window_right=window_right)
 
 
 def _empty_like_layout(ref: torch.Tensor, last_dim: int) -> torch.Tensor:
@@ -71,12 +71,12 @@ def attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, caus
                       scale: Optional[float] = None, sink: Optional[torch.Tensor] = None,
                       cu_seqlens: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
                       cu_seqlens_k: Optional[torch.Tensor] = None, max_seqlen_k: Optional[int] = None,
-                      workspace: Optional[torch.Tensor] = None):
+                      window_right: int = 0, workspace: Optional[torch.Tensor] = None):
     """Returns (o, lse): o [B,Hq,S,Dv] in q's dtype, lse [B,Hq,S] fp32 (natural log, sink included)."""
     B, Hq, S, _ = q.shape
     o = _empty_like_layout(q, v.shape[3])
     p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, cu_seqlens_k=cu_seqlens_k,
-                max_seqlen_k=max_seqlen_k, o=o)
+                max_seqlen_k=max_seqlen_k, window_right=window_right, o=o)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     ws = workspace if workspace is not None else native.alloc_workspace(p, q.device)
     native.fwd(p, q, k, v, sink, o, lse, ws)
@@ -89,7 +89,8 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                        max_seqlen: Optional[int] = None, group_mode: int = GQA_GROUP_TMEM,
                        red_mode: Optional[int] = None, deterministic: bool = False,
                        cu_seqlens_k: Optional[torch.Tensor] = None, max_seqlen_k: Optional[int] = None,
-                       workspace: Optional[torch.Tensor] = None, out: Optional[dict] = None) -> dict:
+                       window_right: int = 0, workspace: Optional[torch.Tensor] = None,
+                       out: Optional[dict] = None) -> dict:
     """Returns dict(dq, dk, dv, delta[, dsink]).  `out` may hold preallocated tensors of the same names.
     red_mode None picks :func:`preferred_red_mode`."""
     B, Hq, S, Dqk = q.shape
@@ -103,8 +104,8 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
     if "dv" not in res:
         res["dv"] = _empty_like_layout(v, Dv)
     p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode, red_mode, deterministic,
-                cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, o=o, do=dout, dq=res["dq"], dk=res["dk"],
-                dv=res["dv"])
+                cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k, window_right=window_right, o=o, do=dout,
+                dq=res["dq"], dk=res["dk"], dv=res["dv"])
     if "delta" not in res:
         res["delta"] = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
     if sink is not None and "dsink" not in res:
@@ -124,13 +125,14 @@ class GqaAttentionFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic, cu_seqlens_k=None,
-                max_seqlen_k=None):
+                max_seqlen_k=None, window_right=0):
         o, lse = attention_forward(q, k, v, causal=causal, window=window, scale=scale, sink=sink,
                                    cu_seqlens=cu_seqlens, max_seqlen=max_seqlen, cu_seqlens_k=cu_seqlens_k,
-                                   max_seqlen_k=max_seqlen_k)
+                                   max_seqlen_k=max_seqlen_k, window_right=window_right)
         ctx.save_for_backward(q, k, v, o, lse, sink)
         ctx.opts = dict(causal=causal, window=window, scale=scale, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
-                        deterministic=deterministic, cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k)
+                        deterministic=deterministic, cu_seqlens_k=cu_seqlens_k, max_seqlen_k=max_seqlen_k,
+                        window_right=window_right)
         return o
 
     @staticmethod
@@ -138,15 +140,15 @@ class GqaAttentionFunction(torch.autograd.Function):
         q, k, v, o, lse, sink = ctx.saved_tensors
         g = attention_backward(q, k, v, o, lse, do.contiguous(), sink=sink, **ctx.opts)
         dsink = g.get("dsink") if sink is not None and ctx.needs_input_grad[3] else None
-        return g["dq"], g["dk"], g["dv"], dsink, None, None, None, None, None, None, None, None
+        return g["dq"], g["dk"], g["dv"], dsink, None, None, None, None, None, None, None, None, None
 
 
 def gqa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = True, window: int = 0,
                   scale: Optional[float] = None, sink: Optional[torch.Tensor] = None,
                   cu_seqlens: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
                   deterministic: bool = False, cu_seqlens_k: Optional[torch.Tensor] = None,
-                  max_seqlen_k: Optional[int] = None) -> torch.Tensor:
+                  max_seqlen_k: Optional[int] = None, window_right: int = 0) -> torch.Tensor:
     """Differentiable grouped-query attention: returns O [B,Hq,S,Dv]; ``O.backward(dO)`` fills
     q.grad, k.grad, v.grad (and sink.grad, fp32) through the backward kernels."""
     return GqaAttentionFunction.apply(q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic,
-                                      cu_seqlens_k, max_seqlen_k)
+                                      cu_seqlens_k, max_seqlen_k, window_right)

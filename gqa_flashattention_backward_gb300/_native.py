@@ -58,6 +58,7 @@ class Params(ctypes.Structure):
         ("red_mode", ctypes.c_int), ("deterministic", ctypes.c_int),
     ] + [(n, Stride) for n in STRIDE_FIELDS] + [
         ("Sk", ctypes.c_int), ("cu_seqlens_k", ctypes.c_void_p), ("max_seqlen_k", ctypes.c_int),
+        ("window_right", ctypes.c_int),
     ]
 
 
@@ -130,7 +131,7 @@ def _check(status: int, what: str):
 
 def make_params(B, Hq, Hkv, S, Dqk, Dv, dtype, causal=True, window=0, scale=None, cu_seqlens=None,
                 max_seqlen=None, group_mode=GQA_GROUP_TMEM, red_mode=GQA_RED_V4, deterministic=False,
-                strides=None, Sk=None, cu_seqlens_k=None, max_seqlen_k=None) -> Params:
+                strides=None, Sk=None, cu_seqlens_k=None, max_seqlen_k=None, window_right=0) -> Params:
     """Build the parameter struct.  `dtype` is a torch dtype (float16/bfloat16);
     `cu_seqlens` a device int32 tensor or None; `strides` maps some of "q", "k", "v", "o", "do",
     "dq", "dk", "dv" to (batch, head, sequence) element strides (missing: contiguous BHSD)."""
@@ -154,6 +155,7 @@ def make_params(B, Hq, Hkv, S, Dqk, Dv, dtype, causal=True, window=0, scale=None
     p.Sk = int(Sk) if Sk is not None and int(Sk) != int(S) else 0
     p.cu_seqlens_k = cu_seqlens_k.data_ptr() if cu_seqlens_k is not None else None
     p.max_seqlen_k = int(max_seqlen_k) if max_seqlen_k is not None else 0
+    p.window_right = int(window_right)
     for name, st in (strides or {}).items():
         s = getattr(p, name + "_st")
         s.b, s.h, s.s = (int(x) for x in st)

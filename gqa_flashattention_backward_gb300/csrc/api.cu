@@ -79,7 +79,8 @@ gqa_status validate(const gqa_attn_params* p) {
   if (p->Hq % p->Hkv != 0) return GQA_ERR_INVALID_ARG;
   if (p->dtype != GQA_F16 && p->dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return GQA_ERR_INVALID_ARG;
-  if (p->window > 0 && !p->causal) return GQA_ERR_INVALID_ARG;
+  if (p->window > 0 && !p->causal && p->window_right <= 0) return GQA_ERR_INVALID_ARG;
+  if (p->window_right > 0 && p->causal) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(p->scale) || !(p->scale > 0.f)) return GQA_ERR_INVALID_ARG;
   if (p->Sk < 0 || p->max_seqlen_k < 0) return GQA_ERR_INVALID_ARG;
   if (p->cu_seqlens_k && !p->cu_seqlens) return GQA_ERR_INVALID_ARG;
@@ -137,6 +138,7 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   pr.G = p->Hq / p->Hkv;
   pr.causal = p->causal;
   pr.window = p->window > 0 ? p->window : 0;
+  pr.right = p->causal ? 1 : (p->window_right > 0 ? p->window_right : 0);
   pr.scale = p->scale;
   pr.scale_log2 = p->scale * kLog2e;
   pr.cu_seqlens = p->cu_seqlens;

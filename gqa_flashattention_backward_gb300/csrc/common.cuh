@@ -30,6 +30,7 @@ struct Strides {
 struct Problem {
   int B, Hq, Hkv, S, Dqk, Dv, G;  // G = Hq / Hkv
   int causal, window;
+  int right;          // right extent: keys with j - (i + off) < right; 1 = causal, <= 0 = unlimited
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e): logits are exponentiated with ex2
   const int32_t* cu_seqlens;  // device [nseqs+1] or null (dense)
@@ -113,15 +114,12 @@ __device__ __forceinline__ bool load_kseq(const Problem& p, int s, Seq& k) {
   return true;
 }
 
-// Is key j (local) visible to query i (local)?  off = Lk - Lq aligns the causal diagonal at the
-// bottom right (0 when a sequence has as many keys as queries).
-__host__ __device__ __forceinline__ bool visible(int i, int j, int len_k, int off, int causal, int window) {
-  return j < len_k && (!causal || j <= i + off) && (window <= 0 || i + off - j < window);
-}
-// The same test from the pair's diagonal distance d = i + off - j and whether key j exists: the
-// tile loops hoist everything but a compile-time offset into d, two comparisons per element.
-__device__ __forceinline__ bool visible_d(int d, bool key_exists, int causal, int window) {
-  return key_exists && (!causal || d >= 0) && (window <= 0 || d < window);
+// Visibility of key j (local) to query i (local) is decided on the pair's diagonal distance
+// d = i + off - j, off = Lk - Lq aligning the causal diagonal at the bottom right (0 when a sequence
+// has as many keys as queries): the key exists, d > -right (right = 1: causal) and d < window.
+// The tile loops hoist everything but a compile-time offset into d: two comparisons per element.
+__device__ __forceinline__ bool visible_d(int d, bool key_exists, int right, int window) {
+  return key_exists && (right <= 0 || d > -right) && (window <= 0 || d < window);
 }
 
 // Index of the first float of a stats tile: head h, sequence s, 128-row tile t.
@@ -166,17 +164,12 @@ __host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Sk, int Dq
 
 // Query rows that can see some key of the 128-row KV tile kt, as a range of query tiles of
 // `bq` rows: [*t0, *t1).
-__host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len_q, int len_k, int bq, int causal,
+__host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len_q, int len_k, int bq, int right,
                                                              int window, int* t0, int* t1) {
   const int ntq = (len_q + bq - 1) / bq;
-  if (!causal) {
-    *t0 = 0;
-    *t1 = ntq;
-    return;
-  }
   const long long off = static_cast<long long>(len_k) - len_q;
   const long long j_lo = static_cast<long long>(kt) * 128;
-  const long long i_first = j_lo - off;  // first row whose diagonal reaches the tile
+  const long long i_first = right > 0 ? j_lo - off - right + 1 : 0;  // first row reaching the tile
   int a = i_first > 0 ? static_cast<int>(i_first / bq) : 0;
   if (a > ntq) a = ntq;
   int b = ntq;
@@ -190,18 +183,16 @@ __host__ __device__ __forceinline__ void q_tiles_for_kv_tile(int kt, int len_q, 
 }
 
 // Key tiles of `bk` rows visible to the query tile qt of 128 rows: [*k0, *k1).
-__host__ __device__ __forceinline__ void kv_tiles_for_q_tile(int qt, int len_q, int len_k, int bk, int causal,
+__host__ __device__ __forceinline__ void kv_tiles_for_q_tile(int qt, int len_q, int len_k, int bk, int right,
                                                              int window, int* k0, int* k1) {
   const int ntk = (len_k + bk - 1) / bk;
-  if (!causal) {
-    *k0 = 0;
-    *k1 = ntk;
-    return;
-  }
   const long long off = static_cast<long long>(len_k) - len_q;
   const long long d_lo = static_cast<long long>(qt) * 128 + off, d_hi = d_lo + 127;  // diagonals of the tile
-  int b = d_hi < 0 ? 0 : static_cast<int>(d_hi / bk + 1);
-  if (b > ntk) b = ntk;
+  int b = ntk;
+  if (right > 0) {
+    const long long j_hi = d_hi + right - 1;  // last key the tile's last row sees
+    b = j_hi < 0 ? 0 : (j_hi / bk + 1 < ntk ? static_cast<int>(j_hi / bk + 1) : ntk);
+  }
   int a = 0;
   if (window > 0) {
     const long long j_lo = d_lo - window + 1;

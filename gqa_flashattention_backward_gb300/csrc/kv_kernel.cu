@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(448, 1)
     return;
   }
   int t0, t1;
-  q_tiles_for_kv_tile(kt, sq.len, sk.len, C::BQ, p.causal, p.window, &t0, &t1);
+  q_tiles_for_kv_tile(kt, sq.len, sk.len, C::BQ, p.right, p.window, &t0, &t1);
   const int nt = t1 - t0;
   const int g = group_tmem ? head : head / p.G;
   const int nh = group_tmem ? p.G : 1;
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(448, 1)
       const int st = it % C::ST;
       const int t = t0 + it % nt;
       const int i0 = t * C::BQ;
-      const bool need_mask = (j0 + C::BK > sk.len) || (p.causal && i0 + off < j0 + C::BK - 1) ||
+      const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && i0 + off + p.right < j0 + C::BK) ||
                              (p.window > 0 && i0 + C::BQ - 1 + off - j0 >= p.window);
       const float4* sL4 = reinterpret_cast<const float4*>(smem + C::OFF_LSE) + (st * C::BQ + cbase) / 4;
       const float4* sD4 = reinterpret_cast<const float4*>(smem + C::OFF_DEL) + (st * C::BQ + cbase) / 4;
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(448, 1)
           const int d0 = i0 + cbase + 32 * c + off - j;  // diagonal distance of this chunk's first query
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (!visible_d(d0 + e, j < sk.len, p.causal, p.window)) pk[16 * c + e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+            if (!visible_d(d0 + e, j < sk.len, p.right, p.window)) pk[16 * c + e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
         }
         uint32_t pc[16];
 #pragma unroll

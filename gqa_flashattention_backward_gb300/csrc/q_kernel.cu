@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(320, 1)
   const int t = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tiles first
   if (t >= ntq) return;
   int k0, k1;
-  kv_tiles_for_q_tile(t, sq.len, sk.len, C::BK, p.causal, p.window, &k0, &k1);
+  kv_tiles_for_q_tile(t, sq.len, sk.len, C::BK, p.right, p.window, &k0, &k1);
   const int n = k1 - k0;
   const int NIT = FWD ? 2 * n : n;
   const int g = h / p.G;
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int it = w, k = 0; it < NIT; it += 2, ++k) {
         const int kt = k0 + it % n;
         const int j0 = kt * C::BK;
-        const bool need_mask = (j0 + C::BK > sk.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ + off) ||
+        const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && j0 + C::BK > t * C::BQ + off + p.right) ||
                                (p.window > 0 && t * C::BQ + C::BQ - 1 + off - j0 >= p.window);
         if (it >= n && !combined) combine();
         if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(320, 1)
             float a = __uint_as_float(v[e]), b = __uint_as_float(v[e + 1]);
             if (need_mask) {
               const int d0 = il + off - j0;  // diagonal distance to this tile's first key
-              if (!visible_d(d0 - e, j0 + e < sk.len, p.causal, p.window)) a = -INFINITY;
-              if (!visible_d(d0 - e - 1, j0 + e + 1 < sk.len, p.causal, p.window)) b = -INFINITY;
+              if (!visible_d(d0 - e, j0 + e < sk.len, p.right, p.window)) a = -INFINITY;
+              if (!visible_d(d0 - e - 1, j0 + e + 1 < sk.len, p.right, p.window)) b = -INFINITY;
             }
             c0 = fmaxf(c0, a);
             c1 = fmaxf(c1, b);
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(320, 1)
           if (need_mask) {
 #pragma unroll
             for (int e = 0; e < C::BK; ++e)
-              if (!visible_d(il + off - j0 - e, j0 + e < sk.len, p.causal, p.window))
+              if (!visible_d(il + off - j0 - e, j0 + e < sk.len, p.right, p.window))
                 pk[e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
           }
           uint32_t p0[16], p1[16];
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int it = w, k = 0; it < NIT; it += 2, ++k) {
         const int kt = k0 + it;
         const int j0 = kt * C::BK;
-        const bool need_mask = (j0 + C::BK > sk.len) || (p.causal && j0 + C::BK - 1 > t * C::BQ + off) ||
+        const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && j0 + C::BK > t * C::BQ + off + p.right) ||
                                (p.window > 0 && t * C::BQ + C::BQ - 1 + off - j0 >= p.window);
         if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
           ok = false;
@@ -395,8 +395,8 @@ __global__ void __launch_bounds__(320, 1)
             float pb = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, nlse2));
             if (need_mask) {
               const int d0 = il + off - j0 - c0;  // diagonal distance to this chunk's first key
-              if (!visible_d(d0 - 2 * e, j0 + c0 + 2 * e < sk.len, p.causal, p.window)) pa = 0.f;
-              if (!visible_d(d0 - 2 * e - 1, j0 + c0 + 2 * e + 1 < sk.len, p.causal, p.window)) pb = 0.f;
+              if (!visible_d(d0 - 2 * e, j0 + c0 + 2 * e < sk.len, p.right, p.window)) pa = 0.f;
+              if (!visible_d(d0 - 2 * e - 1, j0 + c0 + 2 * e + 1 < sk.len, p.right, p.window)) pb = 0.f;
             }
             const float da = pa * (__uint_as_float(dv[2 * e]) + ndlt);
             const float db = pb * (__uint_as_float(dv[2 * e + 1]) + ndlt);

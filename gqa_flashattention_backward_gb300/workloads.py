@@ -51,6 +51,7 @@ class Workload:
     extra: dict = field(default_factory=dict)
     Sk: Optional[int] = None                      # key rows (or packed key tokens); None: S
     varlen_lengths_k: Optional[List[int]] = None  # per-sequence key counts; None: varlen_lengths
+    window_right: int = 0                         # > 0 (not causal): right extent of a local window
 
     @property
     def key_len(self) -> int:

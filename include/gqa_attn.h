@@ -100,7 +100,8 @@ typedef struct {
                             queries and Lk keys: the diagonal aligned at the bottom right, i.e.
                             j <= i when Lq == Lk (query rows that see no key get O = 0, LSE = -inf
                             or the sink alone, and zero gradients) */
-  int window;            /* > 0: also require i + (Lk - Lq) - j < window (requires causal); <= 0: none */
+  int window;            /* > 0: also require i + (Lk - Lq) - j < window (requires causal or
+                            window_right > 0); <= 0: none */
   float scale;           /* softmax scale on Q.K^T, finite and > 0; typically 1/sqrt(Dqk) */
   const int32_t* cu_seqlens; /* DEVICE int32 [nseq+1], cu[0] = 0, non-decreasing, cu[nseq] = S;
                                 NULL for dense batches.  Requires B == 1. */
@@ -124,6 +125,9 @@ typedef struct {
                                   rules as cu_seqlens, cu[nseq] = Sk), or NULL: the same offsets
                                   as cu_seqlens; requires cu_seqlens */
   int max_seqlen_k;      /* upper bound on every packed key length; 0: max_seqlen */
+  int window_right;      /* > 0 (requires causal == 0): also require j - (i + Lk - Lq) < window_right,
+                            a local window on the right of the diagonal (with window: two-sided);
+                            <= 0: none */
 } gqa_attn_params;
 
 /* Bytes of workspace every call below needs for `p` (0 if `p` is invalid).  The

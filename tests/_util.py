@@ -31,7 +31,8 @@ def assert_close(name, got, ref, rtol=RTOL_MAX, atol=ATOL):
 
 def problem_of(w) -> orc.Problem:
     return orc.Problem(B=w.B, Hq=w.Hq, Hkv=w.Hkv, S=w.S, Dqk=w.Dqk, Dv=w.Dv, causal=w.causal, window=w.window,
-                       scale=w.resolved_scale, cu_seqlens=w.cu_seqlens, Sk=w.key_len, cu_seqlens_k=w.cu_seqlens_k)
+                       scale=w.resolved_scale, cu_seqlens=w.cu_seqlens, Sk=w.key_len, cu_seqlens_k=w.cu_seqlens_k,
+                       window_right=w.window_right)
 
 
 def gpu_run(w, inputs, *, group_mode=nat.GQA_GROUP_TMEM, red_mode=None, deterministic=False,
@@ -45,7 +46,7 @@ def gpu_run(w, inputs, *, group_mode=nat.GQA_GROUP_TMEM, red_mode=None, determin
     cuk = torch.tensor(w.cu_seqlens_k, dtype=torch.int32, device=dev) if w.cu_seqlens_k is not None else None
     kw = dict(causal=w.causal, window=w.window, scale=w.resolved_scale, sink=sd, cu_seqlens=cu,
               max_seqlen=w.max_seqlen if cu is not None else None, cu_seqlens_k=cuk,
-              max_seqlen_k=w.max_seqlen_k if cuk is not None else None)
+              max_seqlen_k=w.max_seqlen_k if cuk is not None else None, window_right=w.window_right)
     o, lse = attention_forward(qd, kd, vd, **kw)
     if o_lse is not None:  # isolate the backward: feed it the oracle's O (rounded) and LSE
         o = torch.as_tensor(o_lse[0]).to(w.dtype).to(dev).contiguous()

@@ -60,3 +60,36 @@ def test_cross_lengths_other_modes(case, mode):
     ref = oracle_full(w, inputs)
     kw = dict(deterministic=True) if mode == "deterministic" else dict(group_mode=nat.GQA_GROUP_ATOMIC)
     _compare(w, gpu_run(w, inputs, **kw), ref)
+
+
+# ---------------------------------------------------------------- right window (non-causal local attention)
+LOCAL = {
+    "twosided64": lambda: W.Workload("l_two64", 50, B=2, Hq=4, Hkv=2, S=300, Dqk=64, Dv=64, dtype=torch.float16,
+                                     causal=False, window=65, window_right=40),
+    "rightonly128_sink": lambda: W.Workload("l_right128", 51, B=1, Hq=4, Hkv=2, S=260, Dqk=128, Dv=128,
+                                            dtype=torch.bfloat16, causal=False, window_right=100, sink=True),
+    "twosided64_prefill": lambda: W.Workload("l_two64x", 52, B=1, Hq=4, Hkv=1, S=200, Sk=330, Dqk=64, Dv=64,
+                                             dtype=torch.float16, causal=False, window=80, window_right=50),
+    "twosided128_varlen": lambda: W.Workload("l_var128", 53, B=1, Hq=4, Hkv=2, S=207, Sk=260, Dqk=128, Dv=128,
+                                             dtype=torch.bfloat16, causal=False, window=50, window_right=30,
+                                             varlen_lengths=[130, 77], varlen_lengths_k=[200, 60]),
+    "twosided192": lambda: W.Workload("l_two192", 54, B=1, Hq=4, Hkv=1, S=260, Dqk=192, Dv=128,
+                                      dtype=torch.bfloat16, causal=False, window=60, window_right=40, qkv_std=0.5),
+}
+
+
+@pytest.mark.parametrize("case", list(LOCAL))
+def test_right_window(case):
+    w = LOCAL[case]()
+    inputs = W.make_inputs(w)
+    ref = oracle_full(w, inputs)
+    _compare(w, gpu_run(w, inputs), ref)
+
+
+@pytest.mark.parametrize("mode", ["deterministic", "atomic"])
+def test_right_window_other_modes(mode):
+    w = LOCAL["twosided64_prefill"]()
+    inputs = W.make_inputs(w)
+    ref = oracle_full(w, inputs)
+    kw = dict(deterministic=True) if mode == "deterministic" else dict(group_mode=nat.GQA_GROUP_ATOMIC)
+    _compare(w, gpu_run(w, inputs, **kw), ref)
