@@ -411,6 +411,31 @@ def run_gpu(args):
             if cf is not c:
                 del cf
 
+    # small, launch-bound problems: the eager chain of launches against one CUDA-graph replay of it
+    graphs = {}
+    if not args.no_graph:
+        for wg in (W.tiny(), W.shrink(W.sink_window(), name="small_sink_window", B=1, Hq=8, Hkv=2, S=512, window=256)):
+            cg = setup(wg)
+            kwg = dict(causal=wg.causal, window=wg.window, scale=wg.resolved_scale, sink=cg["sink"])
+            gb = pkg.GraphedBackward(cg["q"], cg["k"], cg["v"], cg["o"], cg["lse"], cg["do"], **kwg)
+            nst = 50
+
+            def run_many(fn):
+                for _ in range(args.warmup):
+                    fn()
+                torch.cuda.synchronize()
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                g0.record()
+                for _ in range(nst):
+                    fn()
+                g1.record()
+                torch.cuda.synchronize()
+                return g0.elapsed_time(g1) / nst * 1e3
+
+            graphs[wg.name] = dict(shape=wg.describe(), eager_us_per_step=round(run_many(lambda: step(cg)), 2),
+                                   graph_us_per_step=round(run_many(gb.replay), 2))
+            del cg, gb
+
     line = None
     if rank == 0:
         cpu = None
@@ -428,7 +453,8 @@ def run_gpu(args):
                     flops_per_step_convention=flops_conv, flops_per_step_exact=flops_exact,
                     frac_of_peak_exact=round(flops_exact / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clocks,
-                    variants=variants, sweep=sweep, configs=configs, forward=forward)
+                    variants=variants, sweep=sweep, configs=configs, forward=forward,
+                    graph=graphs)
         print(json.dumps(line), flush=True)
     ranks.close()
     return line
@@ -511,6 +537,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--no-forward", action="store_true", help="skip the forward timings")
+    ap.add_argument("--no-graph", action="store_true", help="skip the eager / CUDA-graph comparison")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -10,6 +10,8 @@ the C ABI prescribes:
   ``gqa_attn_bwd_postprocess`` and (with a sink) ``gqa_attn_dsink``.
 * :func:`gqa_attention` -> both, as a ``torch.autograd.Function`` (O from the
   forward, dQ / dK / dV / dsink from the backward when autograd asks for them).
+* :class:`GraphedBackward` -> the backward chain of fixed shapes captured once as a
+  CUDA graph and replayed with one launch (small, launch-bound problems).
 
 Tensors have shape q [B,Hq,S,Dqk], k [B,Hkv,S,Dqk], v [B,Hkv,S,Dv], o/dout [B,Hq,S,Dv]
 and any layout whose head dim is contiguous (BHSD, a BSHD view ``x.transpose(1, 2)``, packed
@@ -28,7 +30,8 @@ from ._native import (GQA_GROUP_ATOMIC, GQA_GROUP_TMEM, GQA_RED_BULK, GQA_RED_NO
                       GQA_RED_V4, GqaError)
 
 __all__ = [
-    "attention_forward", "attention_backward", "gqa_attention", "GqaAttentionFunction", "preferred_red_mode", "native", "GqaError", "GQA_GROUP_TMEM", "GQA_GROUP_ATOMIC",
+    "attention_forward", "attention_backward", "gqa_attention", "GqaAttentionFunction", "GraphedBackward",
+    "preferred_red_mode", "native", "GqaError", "GQA_GROUP_TMEM", "GQA_GROUP_ATOMIC",
     "GQA_RED_V4", "GQA_RED_BULK", "GQA_RED_SCALAR", "GQA_RED_NONE",
 ]
 
@@ -152,3 +155,45 @@ def gqa_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: 
     q.grad, k.grad, v.grad (and sink.grad, fp32) through the backward kernels."""
     return GqaAttentionFunction.apply(q, k, v, sink, causal, window, scale, cu_seqlens, max_seqlen, deterministic,
                                       cu_seqlens_k, max_seqlen_k, window_right)
+
+
+class GraphedBackward:
+    """The backward of fixed shapes (preprocess, main kernel, postprocess and, with a sink, the sink
+    gradient) captured once as a CUDA graph; :meth:`replay` runs all of it with one graph launch on
+    the current stream.  The graph reads and writes the very tensors it was built with: copy new
+    q, k, v, o, lse, dout (and sink) into them in place before a replay; the results are in
+    :attr:`out` (dq, dk, dv, delta[, dsink]).  Keyword arguments are those of attention_backward."""
+
+    def __init__(self, q, k, v, o, lse, dout, **kw):
+        if "out" in kw or "workspace" in kw:
+            raise ValueError("GraphedBackward owns its outputs and workspace")
+        self.tensors = (q, k, v, o, lse, dout)
+        self.kw = kw  # keeps sink / cu_seqlens alive: the graph holds their addresses
+        B, Hq, S, Dqk = q.shape
+        self.out = dict(dq=_empty_like_layout(q, Dqk), dk=_empty_like_layout(k, Dqk),
+                        dv=_empty_like_layout(v, v.shape[3]),
+                        delta=torch.empty((B, Hq, S), dtype=torch.float32, device=q.device))
+        if kw.get("sink") is not None:
+            self.out["dsink"] = torch.empty((Hq,), dtype=torch.float32, device=q.device)
+        p = _params(q, k, v, kw.get("causal", True), kw.get("window", 0), kw.get("scale"), kw.get("cu_seqlens"),
+                    kw.get("max_seqlen"), kw.get("group_mode", GQA_GROUP_TMEM), kw.get("red_mode"),
+                    kw.get("deterministic", False), cu_seqlens_k=kw.get("cu_seqlens_k"),
+                    max_seqlen_k=kw.get("max_seqlen_k"), window_right=kw.get("window_right", 0))
+        self.workspace = native.alloc_workspace(p, q.device)
+        side = torch.cuda.Stream(device=q.device)
+        side.wait_stream(torch.cuda.current_stream(q.device))
+        with torch.cuda.stream(side):  # one eager run first: kernel attributes, lazy module loading
+            self._run()
+        torch.cuda.current_stream(q.device).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        # the library does host-side setup (tensor maps, kernel attributes) between its launches
+        with torch.cuda.graph(self.graph, capture_error_mode="relaxed"):
+            self._run()
+
+    def _run(self):
+        q, k, v, o, lse, dout = self.tensors
+        attention_backward(q, k, v, o, lse, dout, workspace=self.workspace, out=self.out, **self.kw)
+
+    def replay(self) -> dict:
+        self.graph.replay()
+        return self.out
