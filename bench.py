@@ -97,25 +97,35 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
+        self.period = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host monotonic time, csv line)
+        self.window = None  # host times bracketing the timed region
         self._t = None
+        self._first = threading.Event()
 
     def start(self):
+        """Starts sampling and waits (up to 5 s) for the first sample, so the timed region is covered."""
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            self._first.wait(timeout=5.0)
         except Exception:
             self.proc = None
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+            self._first.set()
+
+    def mark(self, t0: float, t1: float):
+        """Host times (after a device synchronize) at the start and the end of the timed region."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -129,7 +139,13 @@ class ClockSampler:
             self._t.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            # samples taken during the timed region (a sample reports the state of its last period)
+            inside = [x for x in lines if self.window[0] <= x[0] <= self.window[1] + self.period * 1e-3]
+            lines = inside if inside else lines
+        scope = "timed region" if self.window is not None and lines is not self.lines else "whole run"
+        for _, ln in lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -143,7 +159,8 @@ class ClockSampler:
                     reasons.add(nm)
         if not sm:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"])
-        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), reasons=sorted(reasons), samples=len(sm))
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), reasons=sorted(reasons), samples=len(sm),
+                    sample_ms=self.period, scope=scope)
 
 
 def _src_hash(*names):
@@ -216,7 +233,7 @@ def run_gpu(args):
             n += 1
         return n
 
-    def timed(c, steps, warmup, main_events=False):
+    def timed(c, steps, warmup, main_events=False, sampler=None):
         for _ in range(warmup):
             step(c)
         torch.cuda.synchronize()
@@ -226,11 +243,14 @@ def run_gpu(args):
             if main_events else [None] * steps
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         launches = 0
+        h0 = time.monotonic()
         t0.record()
         for i in range(steps):
             launches += step(c, evs[i])
         t1.record()
         torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.mark(h0, time.monotonic())
         barrier()
         ms = t0.elapsed_time(t1)
         main_ms = sum(a.elapsed_time(b) for a, b in evs) / steps if main_events else None
@@ -242,7 +262,7 @@ def run_gpu(args):
     c = setup(w)
     sampler = ClockSampler(local)
     sampler.start()
-    total_ms, main_ms, launches = timed(c, args.steps, args.warmup, main_events=True)
+    total_ms, main_ms, launches = timed(c, args.steps, args.warmup, main_events=True, sampler=sampler)
     clocks = sampler.stop()
     total_ms = max_over_ranks(total_ms)
     ms_step = total_ms / args.steps
@@ -507,7 +527,8 @@ def run_reference(args):
     ws_n, rank, _ = _dist()
     if rank != 0:
         return None
-    n, w, timer, _ = _calibrated_sample(1.5)
+    # each step a sample of about 0.4-1.5 s, less when many steps are asked for (the run stays near a minute)
+    n, w, timer, _ = _calibrated_sample(min(1.5, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         timer()
     tot = sum(timer() for _ in range(args.steps))
@@ -527,7 +548,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--n-ctx", type=int, default=HEADLINE_N)

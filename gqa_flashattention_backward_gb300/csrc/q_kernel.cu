@@ -15,11 +15,13 @@
 //         atomics.
 //
 // Warp roles (320 threads): warps 0-3 and 4-7 are two softmax warpgroups that
-// take alternate key tiles (warpgroup w the tiles with index parity w, each with
-// its own TMEM buffer), thread r owns query row r = TMEM lane r; warp 8 = TMA
-// producer; warp 9 = TMEM allocator + MMA issuer (the whole warp runs the loop,
-// one lane elected per MMA).  While one warpgroup works on its tile the tensor
-// core computes the other's, so the softmax and the MMAs overlap.  Operands
+// take alternate key tiles (warpgroup w the tiles with index parity w), thread r
+// owns query row r = TMEM lane r; warp 8 = TMA producer; warp 9 = TMEM allocator
+// + MMA issuer (the whole warp runs the loop, one lane elected per MMA).  Tile
+// `it` has the TMEM buffer it % NBUF: while one warpgroup works on its tile the
+// tensor core computes the other's, and in the forward (four buffers) it already
+// computes each warpgroup's next tile, so a warpgroup that finishes a tile finds
+// the next one waiting.  Operands
 // live in shared memory in the 128-byte swizzled layout TMA writes; S, dP, O,
 // dQ accumulate in TMEM; P / dS are packed to 16 bits in TMEM and feed the next
 // MMA as its A operand.
@@ -44,29 +46,37 @@ struct QCfg {
   // FWD: a 64-column block of ones after V in every stage, so P.[V | 1] also yields sum_j P
   static constexpr int ONES_BYTES = FWD ? BK * 128 : 0;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES + ONES_BYTES;
-  static constexpr int BUDGET = 220 * 1024;
+  // CTAs per SM: the forward of head dim 64 fits two (half the shared memory, a quarter of TMEM
+  // each), whose warps hide each other's latencies; every other variant runs one
+  static constexpr int CTAS = (FWD && DQK == 64) ? 2 : 1;
+  static constexpr int BUDGET = CTAS == 2 ? 110 * 1024 : 220 * 1024;
   static constexpr int KST_RAW = (BUDGET - Q_BYTES - DO_BYTES) / STAGE_BYTES;
-  static constexpr int KST = KST_RAW > 4 ? 4 : KST_RAW;
+  static constexpr int KST = KST_RAW > 8 ? 8 : KST_RAW;
   static constexpr int SMEM = 1024 + Q_BYTES + DO_BYTES + KST * STAGE_BYTES;
-  // TMEM: warpgroup w's buffer at w*BUF holds S (BK columns; P / dS packed over its first
-  // half) and, for DQ, dP right after it; the accumulator (O or dQ) follows both buffers
+  // TMEM: buffer b at b*BUF holds S (BK columns; P / dS packed over its first half) and, for
+  // DQ, dP right after it; the accumulator (O or dQ) follows the NBUF buffers
+  // (the MMA warp issues S of tile it + NBUF before the accumulation of tile it + 1: the key stages
+  // must hold NBUF tiles and then some, or that S waits for a stage that the accumulation of tile
+  // it has only just freed, and the accumulation of tile it + 1 waits behind it)
+  static constexpr int NBUF = (FWD && KST >= 6) ? 4 : 2;
   static constexpr uint32_t BUF = FWD ? BK : 2 * BK;
-  static constexpr uint32_t T_ACC = 2 * BUF;
+  static constexpr uint32_t T_ACC = NBUF * BUF;
   static constexpr uint32_t ACC_COLS = FWD ? DV + 16 : DQK;  // FWD: O and 16 columns of the row sum
   static constexpr uint32_t OUT_COLS = FWD ? DV : DQK;       // columns written out
   static constexpr uint32_t TMEM_COLS = (T_ACC + ACC_COLS <= 256) ? 256 : 512;
   static constexpr int THREADS = 320;
-  static_assert(KST >= 2, "stages");
+  static_assert(KST >= 2 && NBUF <= KST, "stages");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(T_ACC + ACC_COLS <= 512, "tmem");
+  static_assert(CTAS == 1 || (TMEM_COLS <= 256 && SMEM <= 112 * 1024), "two CTAs per SM");
   static_assert(OUT_COLS % 64 == 0, "each warpgroup drains whole 32-column chunks");
 };
 
 struct QSmemCtl {
   uint64_t bar_q;
-  uint64_t kv_full[4], kv_empty[4];
-  uint64_t s_full[2];   // tensor core -> warpgroup w: S (and dP) of its tile are in TMEM
-  uint64_t sm_done[2];  // warpgroup w -> tensor core: S read / P or dS stored, buffer reusable
+  uint64_t kv_full[8], kv_empty[8];
+  uint64_t s_full[4];   // tensor core -> warpgroup: S (and dP) of the buffer's tile are in TMEM
+  uint64_t sm_done[4];  // warpgroup -> tensor core: S read / P or dS stored, buffer reusable
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -75,7 +85,7 @@ struct QSmemCtl {
 
 
 template <int DQK, int DV, bool BF16, bool FWD>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
     q_kernel(const Problem p, const __grid_constant__ Maps m, const float* __restrict__ sink, void* __restrict__ out,
              float* __restrict__ lse_out) {
   using C = QCfg<DQK, DV, FWD>;
@@ -112,7 +122,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&ctl.kv_full[i], 1);
       mbar_init(&ctl.kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(&ctl.s_full[i], 1);
       mbar_init(&ctl.sm_done[i], 4);  // one arrival per warp of the warpgroup
     }
@@ -187,15 +197,16 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t dDO0 = sdesc_sw128(smem_u32(sDO), 16, 1024);  // dO, K-major (A of dP)
       auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
       bool ok = mbar_wait_warp(&ctl.bar_q, 0, guard, 2);
-      // S (and dP) of tile `it` into warpgroup (it & 1)'s buffer
+      // S (and dP) of tile `it` into buffer it % NBUF, once the tile NBUF earlier has left it
       auto issue_s = [&](int it) -> bool {
-        const int st = it % C::KST, w = it & 1;
+        const int st = it % C::KST, b = it % C::NBUF;
         if (!mbar_wait_warp(&ctl.kv_full[st], (it / C::KST) & 1, guard, 3)) return false;
-        if (it >= 2 && !mbar_wait_warp(&ctl.sm_done[w], ((it - 2) >> 1) & 1, guard, 4)) return false;
+        if (it >= C::NBUF && !mbar_wait_warp(&ctl.sm_done[b], ((it - C::NBUF) / C::NBUF) & 1, guard, 4))
+          return false;
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
         const uint64_t dK = sdesc_sw128(aK, 16, 1024);
-        const uint32_t tS = tmem + w * C::BUF;
+        const uint32_t tS = tmem + b * C::BUF;
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk)
           umma_ss(tS, desc_advance(dQ0, kstep(kk, C::BQ)), desc_advance(dK, kstep(kk, C::BK)), idS, kk > 0);
@@ -206,17 +217,17 @@ __global__ void __launch_bounds__(320, 1)
             umma_ss(tS + C::BK, desc_advance(dDO0, kstep(kk, C::BQ)), desc_advance(dV, kstep(kk, C::BK)), idS,
                     kk > 0);
         }
-        umma_commit(&ctl.s_full[w]);
+        umma_commit(&ctl.s_full[b]);
         if (FWD && it < n) umma_commit(&ctl.kv_empty[st]);  // statistics pass: K consumed by S alone
         return true;
       };
-      // FWD: O += P.V; DQ: dQ += dS.K -- A = the packed P / dS in the warpgroup's buffer
+      // FWD: O += P.V; DQ: dQ += dS.K -- A = the packed P / dS in the tile's buffer
       auto issue_acc = [&](int it) -> bool {
-        const int st = it % C::KST, w = it & 1;
-        if (!mbar_wait_warp(&ctl.sm_done[w], (it >> 1) & 1, guard, 5)) return false;
+        const int st = it % C::KST, b = it % C::NBUF;
+        if (!mbar_wait_warp(&ctl.sm_done[b], (it / C::NBUF) & 1, guard, 5)) return false;
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
-        const uint32_t tA = tmem + w * C::BUF;
+        const uint32_t tA = tmem + b * C::BUF;
         const int first = FWD ? n : 0;
         if (FWD) {
           // [V | ones], MN-major (B of P.[V | 1]): the ones block follows V's 64-column blocks
@@ -235,11 +246,12 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit(&ctl.kv_empty[st]);
         return true;
       };
-      if (ok && NIT > 0) ok = issue_s(0);
-      if (ok && NIT > 1) ok = issue_s(1);
+      for (int it = 0; ok && it < C::NBUF && it < NIT; ++it) ok = issue_s(it);
+      // in the order the warpgroups release the buffers: tile it's accumulation, then the
+      // tile that takes its buffer next
       for (int it = 0; ok && it < NIT; ++it) {
         if ((!FWD || it >= n) && !issue_acc(it)) break;
-        if (it + 2 < NIT && !issue_s(it + 2)) break;
+        if (it + C::NBUF < NIT && !issue_s(it + C::NBUF)) break;
       }
       umma_commit(&ctl.acc_done);
     }
@@ -249,7 +261,6 @@ __global__ void __launch_bounds__(320, 1)
     const int r = tid & 127;  // query row within the tile == TMEM lane
     const int il = t * C::BQ + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + w * C::BUF;
     const float sl2 = p.scale_log2;
     const float2 sl22 = make_float2(sl2, sl2);
     bool ok = true;
@@ -267,13 +278,15 @@ __global__ void __launch_bounds__(320, 1)
         mref = (M == -INFINITY) ? 0.f : M;
         combined = true;
       };
-      for (int it = w, k = 0; it < NIT; it += 2, ++k) {
+      for (int it = w; it < NIT; it += 2) {
         const int kt = k0 + it % n;
         const int j0 = kt * C::BK;
         const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && j0 + C::BK > t * C::BQ + off + p.right) ||
                                (p.window > 0 && t * C::BQ + C::BQ - 1 + off - j0 >= p.window);
         if (it >= n && !combined) combine();
-        if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
+        const int b = it % C::NBUF;
+        const uint32_t tS = tmem + lane_base + b * C::BUF;
+        if (!mbar_wait_warp(&ctl.s_full[b], (it / C::NBUF) & 1, guard, 6)) {
           ok = false;
           break;
         }
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(320, 1)
           tmem_st_wait();
           tc_fence_before();
         }
-        mbar_arrive_warp(&ctl.sm_done[w]);
+        mbar_arrive_warp(&ctl.sm_done[b]);
       }
       if (!combined) combine();  // both warpgroups reach the named barrier exactly once
       // epilogue: l = sum_j P (the ones column) + the sink's term; O = (P.V) / l; LSE = max + log l.
@@ -373,12 +386,14 @@ __global__ void __launch_bounds__(320, 1)
       const size_t sidx = stat_index(p, h, s, t) + r;
       const float nlse2 = p.nlse2[sidx];
       const float ndlt = p.ndelta[sidx];
-      for (int it = w, k = 0; it < NIT; it += 2, ++k) {
+      for (int it = w; it < NIT; it += 2) {
         const int kt = k0 + it;
         const int j0 = kt * C::BK;
         const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && j0 + C::BK > t * C::BQ + off + p.right) ||
                                (p.window > 0 && t * C::BQ + C::BQ - 1 + off - j0 >= p.window);
-        if (!mbar_wait_warp(&ctl.s_full[w], k & 1, guard, 6)) {
+        const int b = it % C::NBUF;
+        const uint32_t tS = tmem + lane_base + b * C::BUF;
+        if (!mbar_wait_warp(&ctl.s_full[b], (it / C::NBUF) & 1, guard, 6)) {
           ok = false;
           break;
         }
@@ -407,7 +422,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive_warp(&ctl.sm_done[w]);
+        mbar_arrive_warp(&ctl.sm_done[b]);
       }
       // epilogue: dQ (x scale); warpgroup w writes columns [w*DQK/2, (w+1)*DQK/2)
       if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
