@@ -43,16 +43,24 @@ struct QCfg {
   static constexpr int DO_BYTES = FWD ? 0 : BQ * DV * 2;
   static constexpr int K_BYTES = BK * DQK * 2;
   static constexpr int V_BYTES = BK * DV * 2;
-  // FWD: a 64-column block of ones after V in every stage, so P.[V | 1] also yields sum_j P
-  static constexpr int ONES_BYTES = FWD ? BK * 128 : 0;
+  // FWD row sum sum_j P: from the tensor core, a 64-column block of ones after V in every stage
+  // (P.[V | 1]), or -- head dim 128, whose O and 16 more columns would not leave two CTAs room in
+  // TMEM -- added up in fp32 by the softmax warpgroups
+  static constexpr bool SUM_MMA = FWD && DQK != 128;
+  static constexpr int ONES_BYTES = SUM_MMA ? BK * 128 : 0;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES + ONES_BYTES;
-  // CTAs per SM: the forward of head dim 64 fits two (half the shared memory, a quarter of TMEM
-  // each), whose warps hide each other's latencies; every other variant runs one
-  static constexpr int CTAS = (FWD && DQK == 64) ? 2 : 1;
+  // CTAs per SM: the forward of head dims 64 and 128 fits two (half the shared memory and of
+  // TMEM each), whose warps hide each other's latencies; every other variant runs one
+  static constexpr int CTAS = (FWD && DQK <= 128) ? 2 : 1;
   static constexpr int BUDGET = CTAS == 2 ? 110 * 1024 : 220 * 1024;
+  // Key/value staging: one ring of K + V (+ ones) stages; or, where only two such stages would fit
+  // (the forward of head dim 128), separate rings of two K and two V tiles, so the first pass
+  // (K alone) and the P.V of the second do not hold the keys the next S needs
   static constexpr int KST_RAW = (BUDGET - Q_BYTES - DO_BYTES) / STAGE_BYTES;
-  static constexpr int KST = KST_RAW > 8 ? 8 : KST_RAW;
-  static constexpr int SMEM = 1024 + Q_BYTES + DO_BYTES + KST * STAGE_BYTES;
+  static constexpr bool SPLIT = FWD && KST_RAW < 3;
+  static constexpr int KST = SPLIT ? 2 : (KST_RAW > 8 ? 8 : KST_RAW);  // K ring (SPLIT) or K + V ring
+  static constexpr int VST = SPLIT ? 2 : 0;                              // V ring (SPLIT)
+  static constexpr int SMEM = 1024 + Q_BYTES + DO_BYTES + (SPLIT ? KST * K_BYTES + VST * V_BYTES : KST * STAGE_BYTES);
   // TMEM: buffer b at b*BUF holds S (BK columns; P / dS packed over its first half) and, for
   // DQ, dP right after it; the accumulator (O or dQ) follows the NBUF buffers
   // (the MMA warp issues S of tile it + NBUF before the accumulation of tile it + 1: the key stages
@@ -61,7 +69,7 @@ struct QCfg {
   static constexpr int NBUF = (FWD && KST >= 6) ? 4 : 2;
   static constexpr uint32_t BUF = FWD ? BK : 2 * BK;
   static constexpr uint32_t T_ACC = NBUF * BUF;
-  static constexpr uint32_t ACC_COLS = FWD ? DV + 16 : DQK;  // FWD: O and 16 columns of the row sum
+  static constexpr uint32_t ACC_COLS = FWD ? DV + (SUM_MMA ? 16 : 0) : DQK;  // O [and 16 columns of row sum]
   static constexpr uint32_t OUT_COLS = FWD ? DV : DQK;       // columns written out
   static constexpr uint32_t TMEM_COLS = (T_ACC + ACC_COLS <= 256) ? 256 : 512;
   static constexpr int THREADS = 320;
@@ -69,18 +77,21 @@ struct QCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(T_ACC + ACC_COLS <= 512, "tmem");
   static_assert(CTAS == 1 || (TMEM_COLS <= 256 && SMEM <= 112 * 1024), "two CTAs per SM");
+  static_assert(!SPLIT || !SUM_MMA, "the split rings hold no ones block");
   static_assert(OUT_COLS % 64 == 0, "each warpgroup drains whole 32-column chunks");
 };
 
 struct QSmemCtl {
   uint64_t bar_q;
-  uint64_t kv_full[8], kv_empty[8];
+  uint64_t kv_full[8], kv_empty[8];  // K + V stages (K stages of the split rings)
+  uint64_t v_full[2], v_empty[2];    // V stages of the split rings
   uint64_t s_full[4];   // tensor core -> warpgroup: S (and dP) of the buffer's tile are in TMEM
   uint64_t sm_done[4];  // warpgroup -> tensor core: S read / P or dS stored, buffer reusable
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort_flag;
   float stat_m[2][128];  // FWD: each warpgroup's row maxima, combined once
+  float stat_l[2][128];  // FWD without SUM_MMA: each warpgroup's row sums
 };
 
 
@@ -96,6 +107,8 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
   uint8_t* sQ = smem;
   uint8_t* sDO = sQ + C::Q_BYTES;
   uint8_t* sK0 = sDO + C::DO_BYTES;  // stage st: K at sK0 + st*STAGE_BYTES, V right after K
+  uint8_t* sV0 = sK0 + C::KST * C::K_BYTES;  // SPLIT: K stage st at sK0 + st*K_BYTES, V stage at sV0
+  constexpr int K_STRIDE = C::SPLIT ? C::K_BYTES : C::STAGE_BYTES;
 
   const int h = blockIdx.x;
   const int s = blockIdx.z;
@@ -122,6 +135,10 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
       mbar_init(&ctl.kv_full[i], 1);
       mbar_init(&ctl.kv_empty[i], 1);
     }
+    for (int i = 0; i < C::VST; ++i) {
+      mbar_init(&ctl.v_full[i], 1);
+      mbar_init(&ctl.v_empty[i], 1);
+    }
     for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(&ctl.s_full[i], 1);
       mbar_init(&ctl.sm_done[i], 4);  // one arrival per warp of the warpgroup
@@ -134,7 +151,7 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
     tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (FWD) {
+  if (C::SUM_MMA) {
     // the constant ones blocks (TMA never writes them); 1.0 in the input dtype
     const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
     for (int st = 0; st < C::KST; ++st) {
@@ -161,8 +178,34 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
       if (!FWD)
         for (int cb = 0; cb < C::VB; ++cb)
           tma_load_4d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.bar_q, cb * 64, row0, h, sq.b);
-      int issued = 0;
-      for (int it = 0; it < NIT; ++it) {
+      int issued = 0, issued_v = 0;
+      if constexpr (C::SPLIT) {
+        // K of tile i, then V of tile i - 1 (when it is a second-pass tile): the order in which the
+        // MMA warp consumes them (S of tile i + 2 follows P.V of tile i)
+        for (int i = 0; i <= NIT; ++i) {
+          if (i < NIT) {
+            const int st = i % C::KST;
+            if (i >= C::KST && !mbar_wait(&ctl.kv_empty[st], ((i / C::KST) - 1) & 1, guard, 1)) break;
+            uint8_t* sK = sK0 + st * C::K_BYTES;
+            const int krow = sk.start + (k0 + i % n) * C::BK;
+            mbar_expect_tx(&ctl.kv_full[st], C::K_BYTES);
+            for (int cb = 0; cb < C::QB; ++cb)
+              tma_load_4d(sK + cb * (C::BK * 128), &m.k, &ctl.kv_full[st], cb * 64, krow, g, sk.b);
+            issued = i + 1;
+          }
+          const int vi = i - 1 - n;  // second-pass index of tile i - 1 (its key tile is k0 + vi)
+          if (vi >= 0) {
+            const int vs = vi % C::VST;
+            if (vi >= C::VST && !mbar_wait(&ctl.v_empty[vs], ((vi / C::VST) - 1) & 1, guard, 1)) break;
+            uint8_t* sV = sV0 + vs * C::V_BYTES;
+            const int krow = sk.start + (k0 + vi) * C::BK;
+            mbar_expect_tx(&ctl.v_full[vs], C::V_BYTES);
+            for (int cb = 0; cb < C::VB; ++cb)
+              tma_load_4d(sV + cb * (C::BK * 128), &m.v, &ctl.v_full[vs], cb * 64, krow, g, sk.b);
+            issued_v = vi + 1;
+          }
+        }
+      } else for (int it = 0; it < NIT; ++it) {
         const int st = it % C::KST;
         if (it >= C::KST && !mbar_wait(&ctl.kv_empty[st], ((it / C::KST) - 1) & 1, guard, 1)) break;
         const bool need_v = !FWD || it >= n;
@@ -185,13 +228,16 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
         mbar_wait(&ctl.bar_q, 0, g2, 0);
         for (int it = issued - C::KST < 0 ? 0 : issued - C::KST; it < issued; ++it)
           mbar_wait(&ctl.kv_full[it % C::KST], (it / C::KST) & 1, g2, 0);
+        if constexpr (C::SPLIT)
+          for (int vi = issued_v - C::VST < 0 ? 0 : issued_v - C::VST; vi < issued_v; ++vi)
+            mbar_wait(&ctl.v_full[vi % C::VST], (vi / C::VST) & 1, g2, 0);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     {  // the whole warp runs the issue loop; one elected lane issues each MMA
       constexpr uint32_t idS = idesc_f16(128, C::BK, BF16, false, false);
-      constexpr uint32_t idPV = idesc_f16(128, DV + 16, BF16, false, true);  // P.[V | 1]
+      constexpr uint32_t idPV = idesc_f16(128, DV + (C::SUM_MMA ? 16 : 0), BF16, false, true);  // P.[V | 1]
       constexpr uint32_t idDQ = idesc_f16(128, DQK, BF16, false, true);
       const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);    // Q, K-major (A of S)
       const uint64_t dDO0 = sdesc_sw128(smem_u32(sDO), 16, 1024);  // dO, K-major (A of dP)
@@ -204,7 +250,7 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
         if (it >= C::NBUF && !mbar_wait_warp(&ctl.sm_done[b], ((it - C::NBUF) / C::NBUF) & 1, guard, 4))
           return false;
         tc_fence_after();
-        const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
+        const uint32_t aK = smem_u32(sK0 + st * K_STRIDE);
         const uint64_t dK = sdesc_sw128(aK, 16, 1024);
         const uint32_t tS = tmem + b * C::BUF;
 #pragma unroll
@@ -218,20 +264,25 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
                     kk > 0);
         }
         umma_commit(&ctl.s_full[b]);
-        if (FWD && it < n) umma_commit(&ctl.kv_empty[st]);  // statistics pass: K consumed by S alone
+        // statistics pass, or keys of their own ring: K consumed by S alone
+        if (C::SPLIT || (FWD && it < n)) umma_commit(&ctl.kv_empty[st]);
         return true;
       };
       // FWD: O += P.V; DQ: dQ += dS.K -- A = the packed P / dS in the tile's buffer
       auto issue_acc = [&](int it) -> bool {
         const int st = it % C::KST, b = it % C::NBUF;
+        constexpr int VSTN = C::VST > 0 ? C::VST : 1;
+        const int vi = it - n, vs = C::SPLIT ? vi % VSTN : 0;  // SPLIT: V of second-pass tile vi
         if (!mbar_wait_warp(&ctl.sm_done[b], (it / C::NBUF) & 1, guard, 5)) return false;
+        if (C::SPLIT && !mbar_wait_warp(&ctl.v_full[vs], (vi / VSTN) & 1, guard, 8)) return false;
         tc_fence_after();
-        const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
+        const uint32_t aK = smem_u32(sK0 + st * K_STRIDE);
         const uint32_t tA = tmem + b * C::BUF;
         const int first = FWD ? n : 0;
         if (FWD) {
           // [V | ones], MN-major (B of P.[V | 1]): the ones block follows V's 64-column blocks
-          const uint64_t dVmn = sdesc_sw128(aK + C::K_BYTES, C::BK * 128, 1024);
+          const uint32_t aV = C::SPLIT ? smem_u32(sV0 + vs * C::V_BYTES) : aK + C::K_BYTES;
+          const uint64_t dVmn = sdesc_sw128(aV, C::BK * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
             umma_ts(tmem + C::T_ACC, tA + kk * 8, desc_advance(dVmn, kk * 2048), idPV,
@@ -243,7 +294,7 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
             umma_ts(tmem + C::T_ACC, tA + kk * 8, desc_advance(dKmn, kk * 2048), idDQ,
                     (it > first || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&ctl.kv_empty[st]);
+        umma_commit(C::SPLIT ? &ctl.v_empty[vs] : &ctl.kv_empty[st]);
         return true;
       };
       for (int it = 0; ok && it < C::NBUF && it < NIT; ++it) ok = issue_s(it);
@@ -269,6 +320,7 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
       const float sink2 = sink ? __ldg(sink + h) * kLog2e : -INFINITY;
       if (w == 0) mx = sink2;
       float mref = 0.f;  // the row maximum both passes agree on (0 for a row with no allowed key)
+      float lsum = 0.f;  // without SUM_MMA: this warpgroup's share of sum_j P
       bool combined = false;
       // both warpgroups' maxima -> the row maximum (once, before the first output tile)
       auto combine = [&]() {
@@ -313,6 +365,23 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
           // second pass: P = exp2(S*scale*log2e - max) <= 1, packed in place over S
           uint32_t pk[C::BK / 2];
           const float2 nl = make_float2(-mref, -mref);
+          if constexpr (!C::SUM_MMA) {
+            // P in fp32, masked, added up (four partial sums) and packed
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            const int d0 = il + off - j0;  // diagonal distance to this tile's first key
+#pragma unroll
+            for (int e = 0; e < C::BK; e += 2) {
+              const float2 x = fma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl22, nl);
+              float pa = ex2_approx(x.x), pb = ex2_approx(x.y);
+              if (need_mask) {
+                if (!visible_d(d0 - e, j0 + e < sk.len, p.right, p.window)) pa = 0.f;
+                if (!visible_d(d0 - e - 1, j0 + e + 1 < sk.len, p.right, p.window)) pb = 0.f;
+              }
+              s4[(e >> 1) & 3] += pa + pb;
+              pk[e / 2] = pack2<BF16>(pa, pb);
+            }
+            lsum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          } else {
 #pragma unroll
           for (int e = 0; e < C::BK; e += 4) {
             const float2 x0 = fma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl22, nl);
@@ -332,6 +401,7 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
               if (!visible_d(il + off - j0 - e, j0 + e < sk.len, p.right, p.window))
                 pk[e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
           }
+          }
           uint32_t p0[16], p1[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -346,14 +416,20 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
         mbar_arrive_warp(&ctl.sm_done[b]);
       }
       if (!combined) combine();  // both warpgroups reach the named barrier exactly once
-      // epilogue: l = sum_j P (the ones column) + the sink's term; O = (P.V) / l; LSE = max + log l.
-      // warpgroup w writes output columns [w*DV/2, (w+1)*DV/2)
+      float lrow = 0.f;
+      if constexpr (!C::SUM_MMA) {  // the two warpgroups' row sums (again once each, unconditionally)
+        ctl.stat_l[w][r] = lsum;
+        named_bar_sync(1, 256);
+        lrow = ctl.stat_l[0][r] + ctl.stat_l[1][r];
+      }
+      // epilogue: l = sum_j P (the ones column, or the warpgroups' sums) + the sink's term;
+      // O = (P.V) / l; LSE = max + log l.  Warpgroup w writes output columns [w*DV/2, (w+1)*DV/2)
       if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
         tc_fence_after();
         const bool valid = il < sq.len;
         const size_t orow = (static_cast<size_t>(zq) * p.S + sq.start + il);
-        float l = 0.f;
-        if (n > 0) {
+        float l = lrow;
+        if (C::SUM_MMA && n > 0) {
           uint32_t sv[16];
           tmem_ld16(tmem + lane_base + C::T_ACC + DV, sv);
           l = __uint_as_float(sv[0]);
