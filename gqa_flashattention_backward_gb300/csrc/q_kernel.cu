@@ -7,7 +7,8 @@
 //         over the key tiles: the first finds each row's maximum logit (sink
 //         included; no exponentials), the second forms P = exp(S - max) <= 1 and
 //         accumulates P.[V | 1] in TMEM, whose extra column is the row sum l, so
-//         O = (P.V) / l and LSE = max + log l with no rescaling of O.
+//         O = (P.V) / l and LSE = max + log l with no rescaling of O (head dim
+//         128: P.V, with l added up in fp32 by the softmax warpgroups).
 //   DQ  : the query-stationary dQ pass (deterministic mode, and the dQ of head
 //         dim 192): S = Q.K^T, dP = dO.V^T, dS = P*(dP - Delta) (same PR, review
 //         thread k1..k5, in the loop order the Ascend kernel uses for dQ,
