@@ -1,0 +1,21 @@
+// Host driver for the tile-range bookkeeping of the CUDA path (common.cuh): reads lines
+// "kind tile len_q len_k rows right window" from stdin and prints the range "first end" that
+//   kind q: q_tiles_for_kv_tile -- query tiles of `rows` rows that may see the 128-key tile `tile`
+//   kind k: kv_tiles_for_q_tile -- key tiles of `rows` keys that the 128-row query tile `tile` may see
+// The kernels visit only these tiles, so a range that misses a visible tile drops gradient terms.
+#include <cstdio>
+#include "common.cuh"
+
+int main() {
+  char kind;
+  int tile, len_q, len_k, rows, right, window;
+  while (std::scanf(" %c %d %d %d %d %d %d", &kind, &tile, &len_q, &len_k, &rows, &right, &window) == 7) {
+    int a = 0, b = 0;
+    if (kind == 'q')
+      gqa::q_tiles_for_kv_tile(tile, len_q, len_k, rows, right, window, &a, &b);
+    else
+      gqa::kv_tiles_for_q_tile(tile, len_q, len_k, rows, right, window, &a, &b);
+    std::printf("%d %d\n", a, b);
+  }
+  return 0;
+}
