@@ -20,12 +20,12 @@
 // owns query row r = TMEM lane r; warp 8 = TMA producer; warp 9 = TMEM allocator
 // + MMA issuer (the whole warp runs the loop, one lane elected per MMA).  Tile
 // `it` has the TMEM buffer it % NBUF: while one warpgroup works on its tile the
-// tensor core computes the other's, and in the forward (four buffers) it already
-// computes each warpgroup's next tile, so a warpgroup that finishes a tile finds
-// the next one waiting.  Operands
-// live in shared memory in the 128-byte swizzled layout TMA writes; S, dP, O,
-// dQ accumulate in TMEM; P / dS are packed to 16 bits in TMEM and feed the next
-// MMA as its A operand.
+// tensor core computes the other's (NBUF = 2; with four buffers, for a CTA that
+// holds six or more key stages, it would also compute each warpgroup's next
+// tile ahead).  The forward of head dims 64 and 128 runs two CTAs per SM, whose
+// warps fill each other's waits.  Operands live in shared memory in the 128-byte
+// swizzled layout TMA writes; S, dP, O, dQ accumulate in TMEM; P / dS are packed
+// to 16 bits in TMEM and feed the next MMA as its A operand.
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include <type_traits>
