@@ -20,10 +20,9 @@
 // owns query row r = TMEM lane r; warp 8 = TMA producer; warp 9 = TMEM allocator
 // + MMA issuer (the whole warp runs the loop, one lane elected per MMA).  Tile
 // `it` has the TMEM buffer it % NBUF: while one warpgroup works on its tile the
-// tensor core computes the other's (NBUF = 2; with four buffers, for a CTA that
-// holds six or more key stages, it would also compute each warpgroup's next
-// tile ahead).  The forward of head dims 64 and 128 runs two CTAs per SM, whose
-// warps fill each other's waits.  Operands live in shared memory in the 128-byte
+// tensor core computes the other's; with four buffers (the forward of head dim
+// 192) it also computes each warpgroup's next tile ahead.  The forward of head
+// dims 64 and 128 runs two CTAs per SM, whose warps fill each other's waits.  Operands live in shared memory in the 128-byte
 // swizzled layout TMA writes; S, dP, O, dQ accumulate in TMEM; P / dS are packed
 // to 16 bits in TMEM and feed the next MMA as its A operand.
 #include <cuda_fp16.h>
@@ -54,20 +53,26 @@ struct QCfg {
   // TMEM each), whose warps hide each other's latencies; every other variant runs one
   static constexpr int CTAS = (FWD && DQK <= 128) ? 2 : 1;
   static constexpr int BUDGET = CTAS == 2 ? 110 * 1024 : 220 * 1024;
-  // Key/value staging: one ring of K + V (+ ones) stages; or, where only two such stages would fit
-  // (the forward of head dim 128), separate rings of two K and two V tiles, so the first pass
-  // (K alone) and the P.V of the second do not hold the keys the next S needs
+  // Key/value staging: one ring of K + V (+ ones) stages; or, in the forward of head dims 128 (only
+  // two such stages would fit) and 192 (three), separate rings: two V (+ ones) stages and as many
+  // K stages as fit, so the first pass (K alone) and the P.V of the second do not hold the keys the
+  // next S needs
   static constexpr int KST_RAW = (BUDGET - Q_BYTES - DO_BYTES) / STAGE_BYTES;
-  static constexpr bool SPLIT = FWD && KST_RAW < 3;
-  static constexpr int KST = SPLIT ? 2 : (KST_RAW > 8 ? 8 : KST_RAW);  // K ring (SPLIT) or K + V ring
-  static constexpr int VST = SPLIT ? 2 : 0;                              // V ring (SPLIT)
-  static constexpr int SMEM = 1024 + Q_BYTES + DO_BYTES + (SPLIT ? KST * K_BYTES + VST * V_BYTES : KST * STAGE_BYTES);
+  static constexpr bool SPLIT = FWD && (KST_RAW < 3 || DQK == 192);
+  static constexpr int VSTAGE_BYTES = V_BYTES + ONES_BYTES;  // one stage of the V ring
+  static constexpr int VST = SPLIT ? 2 : 0;                  // V ring (SPLIT)
+  static constexpr int KST_SPLIT = (BUDGET - Q_BYTES - DO_BYTES - VST * VSTAGE_BYTES) / K_BYTES;
+  static constexpr int KST = SPLIT ? (KST_SPLIT > 8 ? 8 : KST_SPLIT)    // K ring (SPLIT)
+                                   : (KST_RAW > 8 ? 8 : KST_RAW);       // or K + V ring
+  static constexpr int SMEM =
+      1024 + Q_BYTES + DO_BYTES + (SPLIT ? KST * K_BYTES + VST * VSTAGE_BYTES : KST * STAGE_BYTES);
   // TMEM: buffer b at b*BUF holds S (BK columns; P / dS packed over its first half) and, for
   // DQ, dP right after it; the accumulator (O or dQ) follows the NBUF buffers
   // (the MMA warp issues S of tile it + NBUF before the accumulation of tile it + 1: the key stages
   // must hold NBUF tiles and then some, or that S waits for a stage that the accumulation of tile
-  // it has only just freed, and the accumulation of tile it + 1 waits behind it)
-  static constexpr int NBUF = (FWD && KST >= 6) ? 4 : 2;
+  // it has only just freed, and the accumulation of tile it + 1 waits behind it; keys in a ring of
+  // their own are freed by S alone, so there NBUF stages suffice)
+  static constexpr int NBUF = (FWD && KST >= (SPLIT ? 4 : 6)) ? 4 : 2;
   static constexpr uint32_t BUF = FWD ? BK : 2 * BK;
   static constexpr uint32_t T_ACC = NBUF * BUF;
   static constexpr uint32_t ACC_COLS = FWD ? DV + (SUM_MMA ? 16 : 0) : DQK;  // O [and 16 columns of row sum]
@@ -78,7 +83,6 @@ struct QCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(T_ACC + ACC_COLS <= 512, "tmem");
   static_assert(CTAS == 1 || (TMEM_COLS <= 256 && SMEM <= 112 * 1024), "two CTAs per SM");
-  static_assert(!SPLIT || !SUM_MMA, "the split rings hold no ones block");
   static_assert(OUT_COLS % 64 == 0, "each warpgroup drains whole 32-column chunks");
 };
 
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
   uint8_t* sQ = smem;
   uint8_t* sDO = sQ + C::Q_BYTES;
   uint8_t* sK0 = sDO + C::DO_BYTES;  // stage st: K at sK0 + st*STAGE_BYTES, V right after K
-  uint8_t* sV0 = sK0 + C::KST * C::K_BYTES;  // SPLIT: K stage st at sK0 + st*K_BYTES, V stage at sV0
+  uint8_t* sV0 = sK0 + C::KST * C::K_BYTES;  // SPLIT: K stage st at sK0 + st*K_BYTES, V stages from sV0
   constexpr int K_STRIDE = C::SPLIT ? C::K_BYTES : C::STAGE_BYTES;
 
   const int h = blockIdx.x;
@@ -155,8 +159,9 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
   if (C::SUM_MMA) {
     // the constant ones blocks (TMA never writes them); 1.0 in the input dtype
     const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
-    for (int st = 0; st < C::KST; ++st) {
-      uint4* blk = reinterpret_cast<uint4*>(sK0 + st * C::STAGE_BYTES + C::K_BYTES + C::V_BYTES);
+    for (int st = 0; st < (C::SPLIT ? C::VST : C::KST); ++st) {
+      uint8_t* v = C::SPLIT ? sV0 + st * C::VSTAGE_BYTES : sK0 + st * C::STAGE_BYTES + C::K_BYTES;
+      uint4* blk = reinterpret_cast<uint4*>(v + C::V_BYTES);
       for (int i = tid; i < C::ONES_BYTES / 16; i += C::THREADS) blk[i] = make_uint4(one2, one2, one2, one2);
     }
     fence_async_smem();  // generic-proxy writes read later by the tensor core
@@ -181,9 +186,9 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
           tma_load_4d(sDO + cb * (C::BQ * 128), &m.dout, &ctl.bar_q, cb * 64, row0, h, sq.b);
       int issued = 0, issued_v = 0;
       if constexpr (C::SPLIT) {
-        // K of tile i, then V of tile i - 1 (when it is a second-pass tile): the order in which the
-        // MMA warp consumes them (S of tile i + 2 follows P.V of tile i)
-        for (int i = 0; i <= NIT; ++i) {
+        // K of tile i, then V of tile i - (NBUF - 1) (when it is a second-pass tile): the order in
+        // which the MMA warp consumes them (S of tile i + NBUF follows P.V of tile i)
+        for (int i = 0; i <= NIT + C::NBUF - 2; ++i) {
           if (i < NIT) {
             const int st = i % C::KST;
             if (i >= C::KST && !mbar_wait(&ctl.kv_empty[st], ((i / C::KST) - 1) & 1, guard, 1)) break;
@@ -194,11 +199,11 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
               tma_load_4d(sK + cb * (C::BK * 128), &m.k, &ctl.kv_full[st], cb * 64, krow, g, sk.b);
             issued = i + 1;
           }
-          const int vi = i - 1 - n;  // second-pass index of tile i - 1 (its key tile is k0 + vi)
-          if (vi >= 0) {
+          const int vi = i - (C::NBUF - 1) - n;  // second-pass index of that tile (key tile k0 + vi)
+          if (vi >= 0 && vi < n) {
             const int vs = vi % C::VST;
             if (vi >= C::VST && !mbar_wait(&ctl.v_empty[vs], ((vi / C::VST) - 1) & 1, guard, 1)) break;
-            uint8_t* sV = sV0 + vs * C::V_BYTES;
+            uint8_t* sV = sV0 + vs * C::VSTAGE_BYTES;
             const int krow = sk.start + (k0 + vi) * C::BK;
             mbar_expect_tx(&ctl.v_full[vs], C::V_BYTES);
             for (int cb = 0; cb < C::VB; ++cb)
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(320, (QCfg<DQK, DV, FWD>::CTAS))
         const int first = FWD ? n : 0;
         if (FWD) {
           // [V | ones], MN-major (B of P.[V | 1]): the ones block follows V's 64-column blocks
-          const uint32_t aV = C::SPLIT ? smem_u32(sV0 + vs * C::V_BYTES) : aK + C::K_BYTES;
+          const uint32_t aV = C::SPLIT ? smem_u32(sV0 + vs * C::VSTAGE_BYTES) : aK + C::K_BYTES;
           const uint64_t dVmn = sdesc_sw128(aV, C::BK * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk)
