@@ -137,6 +137,10 @@ class ClockSampler:
             self.proc.kill()
         if self._t:
             self._t.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        """Median SM clock, maximum clock and throttle reasons of the samples in the timed region."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         lines = self.lines
