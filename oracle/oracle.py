@@ -23,6 +23,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gqa_oracle.c")
 _LIB = os.path.join(_HERE, "libgqa_oracle.so")
+# Another build of gqa_oracle.c to load instead of the one above: the mutation test points this at
+# copies with a mistake planted in them and checks that the oracle's pins reject every one.
+_LIB_OVERRIDE = os.environ.get("GQA_ORACLE_LIB")
 
 
 def build_oracle(force: bool = False) -> str:
@@ -50,7 +53,7 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build_oracle())
+        _lib = ctypes.CDLL(_LIB_OVERRIDE or build_oracle())
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int32)
         pp = ctypes.POINTER(_Problem)
