@@ -142,3 +142,17 @@ def test_tensor_strides_of_common_layouts():
     assert nat.tensor_strides(torch.empty(B, H, S, D)) == (H * S * D, S * D, D)
     with pytest.raises(ValueError):
         nat.tensor_strides(torch.empty(B, H, D, S).transpose(2, 3))  # head dim not contiguous
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No CPU fallback: without the compiled library loading raises, and CPU tensors are refused."""
+    import torch
+
+    import gqa_flashattention_backward_gb300 as pkg
+    monkeypatch.setattr(nat, "_LIB_PATH", str(tmp_path / "libgqa_attn.so"))
+    monkeypatch.setattr(nat, "_lib", None)
+    with pytest.raises(ImportError):
+        nat.load()
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        pkg.attention_forward(q, q[:, :1], q[:, :1])
