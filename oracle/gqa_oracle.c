@@ -306,3 +306,99 @@ void oracle_sample_cols(const oracle_problem* p, const double* q, const double* 
     free(orow);
   }
 }
+
+/*
+ * Row statistics at listed query rows (b, h, i): LSE_i from its definition and
+ * Delta_i = dO_i . O_i with O_i = sum_j P_ij V_j -- the values oracle_forward
+ * and oracle_delta give for those rows.  The row's logits are formed once and
+ * kept for the maximum, the sum and the O passes (the same values and the same
+ * order of every sum as row_lse and oracle_forward), so large problems can be
+ * sampled row by row in parallel.  Outputs in list order: lse[n], delta[n].
+ */
+void oracle_row_stats(const oracle_problem* p, const double* q, const double* k, const double* v,
+                      const double* dout, int n, const int32_t* bs, const int32_t* hs, const int32_t* is,
+                      double* lse, double* delta) {
+  const int G = p->Hq / p->Hkv;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int t = 0; t < n; ++t) {
+    const int b = bs[t], h = hs[t], i = is[t], g = h / G;
+    int lo, hi;
+    key_range(p, i, &lo, &hi);
+    const int nk = hi > lo ? hi - lo : 0;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    double* orow = (double*)malloc(sizeof(double) * (size_t)p->Dv);
+    double m = p->sink ? p->sink[h] : -INFINITY;
+    for (int j = lo; j < hi; ++j) {
+      s[j - lo] = logit(p, q, k, b, h, i, j);
+      if (s[j - lo] > m) m = s[j - lo];
+    }
+    double L = -INFINITY;
+    if (m != -INFINITY) {
+      double z = p->sink ? exp(p->sink[h] - m) : 0.0;
+      for (int j = lo; j < hi; ++j) z += exp(s[j - lo] - m);
+      L = m + log(z);
+    }
+    for (int d = 0; d < p->Dv; ++d) orow[d] = 0.0;
+    for (int j = lo; j < hi; ++j) {
+      const double pij = exp(s[j - lo] - L);
+      const double* vj = row(v, p->Hkv, key_len(p), p->Dv, b, g, j);
+      for (int d = 0; d < p->Dv; ++d) orow[d] += pij * vj[d];
+    }
+    lse[t] = L;
+    delta[t] = dot(row(dout, p->Hq, p->S, p->Dv, b, h, i), orow, p->Dv);
+    free(orow);
+    free(s);
+  }
+}
+
+/*
+ * dK_j and dV_j at listed key rows (b, g, j) given LSE and Delta of the query
+ * rows in full [B, Hq, S] arrays: the column pass of oracle_backward restricted
+ * to the listed keys.  Only the entries of rows that see a listed key are read.
+ */
+void oracle_cols_with_stats(const oracle_problem* p, const double* q, const double* k, const double* v,
+                            const double* dout, const double* lse, const double* delta, int n,
+                            const int32_t* bs, const int32_t* gs, const int32_t* js, double* dk, double* dv) {
+  const int G = p->Hq / p->Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < n; ++t) {
+    const int b = bs[t], g = gs[t], j = js[t];
+    double* dkj = dk + (size_t)t * p->Dqk;
+    double* dvj = dv + (size_t)t * p->Dv;
+    for (int d = 0; d < p->Dqk; ++d) dkj[d] = 0.0;
+    for (int d = 0; d < p->Dv; ++d) dvj[d] = 0.0;
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      for (int i = 0; i < p->S; ++i) {
+        int lo, hi;
+        key_range(p, i, &lo, &hi);
+        if (j < lo || j >= hi) continue;
+        const long r = ((long)b * p->Hq + h) * p->S + i;
+        double pij;
+        const double ds = grad_logit(p, q, k, v, dout, lse[r], delta[r], b, h, i, j, &pij);
+        const double* qi = row(q, p->Hq, p->S, p->Dqk, b, h, i);
+        const double* doi = row(dout, p->Hq, p->S, p->Dv, b, h, i);
+        for (int d = 0; d < p->Dqk; ++d) dkj[d] += ds * qi[d];
+        for (int d = 0; d < p->Dv; ++d) dvj[d] += pij * doi[d];
+      }
+    }
+  }
+}
+
+/* dsink_h = - sum over b, i of exp(sink_h - LSE_i) * Delta_i, given full
+ * [B, Hq, S] LSE and Delta ("Kernel 9: Dsink", tilelang-ascend PR #1638). */
+void oracle_dsink(const oracle_problem* p, const double* lse, const double* delta, double* dsink) {
+  if (!p->sink) {
+    for (int h = 0; h < p->Hq; ++h) dsink[h] = 0.0;
+    return;
+  }
+#pragma omp parallel for schedule(static)
+  for (int h = 0; h < p->Hq; ++h) {
+    double acc = 0.0;
+    for (int b = 0; b < p->B; ++b)
+      for (int i = 0; i < p->S; ++i) {
+        const long r = ((long)b * p->Hq + h) * p->S + i;
+        acc += exp(p->sink[h] - lse[r]) * delta[r];
+      }
+    dsink[h] = -acc;
+  }
+}

@@ -62,6 +62,9 @@ def _load():
         _lib.oracle_delta.argtypes = [pp, dp, dp, dp]
         _lib.oracle_sample_rows.argtypes = [pp, dp, dp, dp, dp, ctypes.c_int, ip, ip, ip, dp, dp, dp, dp]
         _lib.oracle_sample_cols.argtypes = [pp, dp, dp, dp, dp, ctypes.c_int, ip, ip, ip, dp, dp]
+        _lib.oracle_row_stats.argtypes = [pp, dp, dp, dp, dp, ctypes.c_int, ip, ip, ip, dp, dp]
+        _lib.oracle_cols_with_stats.argtypes = [pp, dp, dp, dp, dp, dp, dp, ctypes.c_int, ip, ip, ip, dp, dp]
+        _lib.oracle_dsink.argtypes = [pp, dp, dp, dp]
     return _lib
 
 
@@ -195,3 +198,42 @@ def sample_cols(pb: Problem, q, k, v, dout, bs, gs, js, sink=None):
     lib.oracle_sample_cols(ctypes.byref(st), _dp(q), _dp(k), _dp(v), _dp(dout), n, _ip(bs), _ip(gs), _ip(js),
                            _dp(dk), _dp(dv))
     return dict(dk=dk, dv=dv)
+
+
+def row_stats(pb: Problem, q, k, v, dout, bs, hs, is_, sink=None):
+    """Exact LSE and Delta at the listed query rows (b, h, i) (row-parallel; no dQ)."""
+    lib, keep = _load(), []
+    q, k, v, dout = map(_f64, (q, k, v, dout))
+    st = _mk(pb, sink, keep)
+    bs, hs, is_ = (np.ascontiguousarray(x, dtype=np.int32) for x in (bs, hs, is_))
+    n = len(bs)
+    lse = np.zeros(n)
+    delta = np.zeros(n)
+    lib.oracle_row_stats(ctypes.byref(st), _dp(q), _dp(k), _dp(v), _dp(dout), n, _ip(bs), _ip(hs), _ip(is_),
+                         _dp(lse), _dp(delta))
+    return dict(lse=lse, delta=delta)
+
+
+def cols_with_stats(pb: Problem, q, k, v, dout, lse, delta, bs, gs, js, sink=None):
+    """Exact dK, dV at the listed key rows (b, g, j), given LSE and Delta [B, Hq, S] of (at least)
+    every query row that sees one of them."""
+    lib, keep = _load(), []
+    q, k, v, dout, lse, delta = map(_f64, (q, k, v, dout, lse, delta))
+    st = _mk(pb, sink, keep)
+    bs, gs, js = (np.ascontiguousarray(x, dtype=np.int32) for x in (bs, gs, js))
+    n = len(bs)
+    dk = np.zeros((n, pb.Dqk))
+    dv = np.zeros((n, pb.Dv))
+    lib.oracle_cols_with_stats(ctypes.byref(st), _dp(q), _dp(k), _dp(v), _dp(dout), _dp(lse), _dp(delta), n,
+                               _ip(bs), _ip(gs), _ip(js), _dp(dk), _dp(dv))
+    return dict(dk=dk, dv=dv)
+
+
+def dsink(pb: Problem, lse, delta, sink):
+    """dsink [Hq] from full LSE and Delta [B, Hq, S]."""
+    lib, keep = _load(), []
+    lse, delta = _f64(lse), _f64(delta)
+    st = _mk(pb, sink, keep)
+    out = np.zeros(pb.Hq)
+    lib.oracle_dsink(ctypes.byref(st), _dp(lse), _dp(delta), _dp(out))
+    return out

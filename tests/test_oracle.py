@@ -233,6 +233,44 @@ def test_sampled_matches_full():
         np.testing.assert_allclose(sc["dv"][t], g["dv"][b, gg, j], atol=1e-13)
 
 
+
+@pytest.mark.parametrize("case", [
+    dict(B=1, Hq=4, Hkv=2, S=23, Sk=None, causal=True, window=9, right=0, cu=[0, 10, 10, 23], sink=True),
+    dict(B=2, Hq=6, Hkv=2, S=17, Sk=None, causal=True, window=0, right=0, cu=None, sink=False),
+    dict(B=1, Hq=2, Hkv=1, S=9, Sk=14, causal=True, window=4, right=0, cu=None, sink=True),
+    dict(B=1, Hq=4, Hkv=1, S=12, Sk=None, causal=False, window=3, right=2, cu=None, sink=True),
+])
+def test_row_stats_and_columns_match_full(case):
+    """The row-statistics / column / dsink functions used at full size give exactly what the full
+    passes give (which are pinned above by finite differences, brute force and autograd)."""
+    pb = orc.Problem(B=case["B"], Hq=case["Hq"], Hkv=case["Hkv"], S=case["S"], Dqk=6, Dv=5, causal=case["causal"],
+                     window=case["window"], window_right=case["right"], scale=0.41, cu_seqlens=case["cu"],
+                     Sk=case["Sk"])
+    q, k, v, do, sink = _inputs(pb, seed=21, with_sink=case["sink"])
+    o, lse = orc.forward(pb, q, k, v, sink)
+    g = orc.backward(pb, q, k, v, o, lse, do, sink)
+    rows = [(b, h, i) for b in range(pb.B) for h in range(pb.Hq) for i in range(pb.S)]
+    bs, hs, is_ = zip(*rows)
+    st = orc.row_stats(pb, q, k, v, do, bs, hs, is_, sink)
+    L = st["lse"].reshape(pb.B, pb.Hq, pb.S)
+    D = st["delta"].reshape(pb.B, pb.Hq, pb.S)
+    np.testing.assert_allclose(L, lse, atol=1e-13)
+    np.testing.assert_allclose(D, g["delta"], atol=1e-13)
+    cols = [(b, gg, j) for b in range(pb.B) for gg in range(pb.Hkv) for j in range(pb.key_len)]
+    bs, gs, js = zip(*cols)
+    sc = orc.cols_with_stats(pb, q, k, v, do, L, D, bs, gs, js, sink)
+    np.testing.assert_allclose(sc["dk"].reshape(g["dk"].shape), g["dk"], atol=1e-13)
+    np.testing.assert_allclose(sc["dv"].reshape(g["dv"].shape), g["dv"], atol=1e-13)
+    if sink is not None:
+        np.testing.assert_allclose(orc.dsink(pb, L, D, sink), g["dsink"], atol=1e-13)
+    # the column pass reads only rows that see the key: unrelated rows may hold anything
+    if case["causal"] and case["cu"] is None and case["Sk"] is None:
+        Ln, Dn = L.copy(), D.copy()
+        Ln[:, :, :3], Dn[:, :, :3] = np.nan, np.nan   # rows 0..2 never see key 5 under a causal mask
+        c5 = orc.cols_with_stats(pb, q, k, v, do, Ln, Dn, [0], [0], [5], sink)
+        np.testing.assert_allclose(c5["dk"][0], g["dk"][0, 0, 5], atol=1e-13)
+
+
 def test_empty_sequence_rows_are_untouched():
     # an empty packed sequence contributes no rows; its neighbours are unaffected
     pb1 = orc.Problem(B=1, Hq=2, Hkv=1, S=9, Dqk=4, Dv=4, causal=True, scale=0.5, cu_seqlens=[0, 4, 4, 9])

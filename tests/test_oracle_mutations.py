@@ -15,13 +15,13 @@ SRC = os.path.join(ROOT, "oracle", "gqa_oracle.c")
 
 # name -> [(text in gqa_oracle.c, replacement, expected occurrences)]
 MUTANTS = {
-    "dsink_sign": [("dsink[h] = -acc;", "dsink[h] = acc;", 1)],
+    "dsink_sign": [("dsink[h] = -acc;", "dsink[h] = acc;", 2)],
     "scale_dropped_in_dS": [("return pij * (dpij - D_i) * p->scale;", "return pij * (dpij - D_i);", 1)],
-    "group_map_modulo": [("h / (p->Hq / p->Hkv)", "h % p->Hkv", 2), ("h / G", "h % p->Hkv", 3)],
+    "group_map_modulo": [("h / (p->Hq / p->Hkv)", "h % p->Hkv", 2), ("h / G", "h % p->Hkv", 4)],
     "window_one_key_wider": [("il + off - p->window + 1 > a) a = il + off - p->window + 1;",
                               "il + off - p->window > a) a = il + off - p->window;", 1)],
-    "sink_left_out_of_denominator": [("double z = p->sink ? exp(p->sink[h] - m) : 0.0;", "double z = 0.0;", 1)],
-    "dV_from_dS": [("dvj[d] += pij * doi[d];", "dvj[d] += ds * doi[d];", 2)],
+    "sink_left_out_of_denominator": [("double z = p->sink ? exp(p->sink[h] - m) : 0.0;", "double z = 0.0;", 2)],
+    "dV_from_dS": [("dvj[d] += pij * doi[d];", "dvj[d] += ds * doi[d];", 3)],
     "causal_excludes_diagonal": [("if (p->causal && il + off + 1 < b) b = il + off + 1;",
                                   "if (p->causal && il + off < b) b = il + off;", 1)],
     "causal_top_left_when_lengths_differ": [("off = kl - ql;", "off = 0;", 1)],
