@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 HEADLINE_N = 16384
 SWEEP = (2048, 4096, 8192, 16384, 32768)
+NOMINAL_DENSE_TFLOPS = 2250.0  # NVIDIA's dense fp16 / bf16 tensor figure for GB300
 
 
 def _dist():
@@ -204,22 +205,37 @@ def run_gpu(args):
     nat.load()
     peaks = _peaks()
 
+    inputs_cache = {}
+
+    def case(w):
+        """Inputs on the device and the forward's O / LSE of workload w (made once per workload)."""
+        if w.name not in inputs_cache:
+            q, k, v, do, sink = W.make_inputs(w)
+            q, k, v, do = (t.to(dev) for t in (q, k, v, do))
+            sink = sink.to(dev) if sink is not None else None
+            cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev) if w.cu_seqlens else None
+            kw = dict(causal=w.causal, window=w.window, scale=w.resolved_scale, cu_seqlens=cu,
+                      max_seqlen=w.max_seqlen if cu is not None else None)
+            o, lse = pkg.attention_forward(q, k, v, sink=sink, **kw)
+            inputs_cache[w.name] = dict(w=w, q=q, k=k, v=v, do=do, o=o, lse=lse, sink=sink, cu=cu,
+                                        max_seqlen=kw["max_seqlen"])
+        return inputs_cache[w.name]
+
+    def drop(w):
+        inputs_cache.pop(w.name, None)
+
     def setup(w, red_mode=None, group_mode=nat.GQA_GROUP_TMEM, deterministic=False):
-        q, k, v, do, sink = W.make_inputs(w)
-        q, k, v, do = (t.to(dev) for t in (q, k, v, do))
-        sink = sink.to(dev) if sink is not None else None
-        cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev) if w.cu_seqlens else None
-        kw = dict(causal=w.causal, window=w.window, scale=w.resolved_scale, cu_seqlens=cu,
-                  max_seqlen=w.max_seqlen if cu is not None else None)
-        o, lse = pkg.attention_forward(q, k, v, sink=sink, **kw)
-        p = pkg._params(q, k, v, w.causal, w.window, w.resolved_scale, cu, kw["max_seqlen"], group_mode, red_mode,
-                        deterministic)
+        c = dict(case(w))
+        q, k, v, lse = c["q"], c["k"], c["v"], c["lse"]
+        p = pkg._params(q, k, v, w.causal, w.window, w.resolved_scale, c["cu"], c["max_seqlen"], group_mode,
+                        red_mode, deterministic)
         wsb = nat.alloc_workspace(p, dev)
         out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                    delta=torch.empty(lse.shape, dtype=torch.float32, device=dev))
-        if sink is not None:
+        if c["sink"] is not None:
             out["dsink"] = torch.empty(w.Hq, dtype=torch.float32, device=dev)
-        return dict(w=w, q=q, k=k, v=v, do=do, o=o, lse=lse, sink=sink, p=p, ws=wsb, out=out)
+        c.update(p=p, ws=wsb, out=out)
+        return c
 
     def step(c, ev=None):
         """One backward pass through the C ABI; returns the number of kernels launched."""
@@ -280,6 +296,8 @@ def run_gpu(args):
     traffic = _traffic(f"kv_kernel/{w.name}", src)
     roofline = dict(bound="tensor", achieved=round(achieved, 2), peak=peaks["bf16_tflops"], unit="TFLOP/s",
                     frac=round(achieved / peaks["bf16_tflops"], 4), traffic=traffic,
+                    peak_nominal=NOMINAL_DENSE_TFLOPS, frac_nominal=round(achieved / NOMINAL_DENSE_TFLOPS, 4),
+                    peak_nominal_source="NVIDIA's dense fp16/bf16 tensor figure for GB300 (2.25 PFLOP/s)",
                     kernel="kv_kernel<64,64,fp16>", kernel_ms=round(main_ms, 4),
                     flops_per_launch=flops_exact, peak_source=f"{peaks['source']} bf16 burst (fp16 same rate)")
 
@@ -304,13 +322,19 @@ def run_gpu(args):
             cmp_done[sl].record(s_cmp)
             out_done[sl].record(s_out)
 
-        def e2e_step(i):
+        link_ev = []  # (upload start, upload end, read-back start, read-back end) per timed step
+
+        def e2e_step(i, evs=None):
             sl = i % 2
             with torch.cuda.stream(s_in):
                 s_in.wait_event(cmp_done[sl])  # the backward that last read this input set is done
+                if evs is not None:
+                    evs[0].record(s_in)
                 for n in names_in:
                     dbufs[sl][n].copy_(pinned[n], non_blocking=True)
                 in_done[sl].record(s_in)
+                if evs is not None:
+                    evs[1].record(s_in)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(in_done[sl])
                 s_cmp.wait_event(out_done[sl])  # the read-back of this output set is done
@@ -320,9 +344,13 @@ def run_gpu(args):
                 cmp_done[sl].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(cmp_done[sl])
+                if evs is not None:
+                    evs[2].record(s_out)
                 for n in ("dq", "dk", "dv"):
                     host_out[n].copy_(douts[sl][n], non_blocking=True)
                 out_done[sl].record(s_out)
+                if evs is not None:
+                    evs[3].record(s_out)
 
         def e2e_serial_step():
             for n in names_in:
@@ -342,11 +370,15 @@ def run_gpu(args):
         s_cmp.wait_event(t0)
         s_out.wait_event(t0)
         for i in range(args.steps):
-            e2e_step(i)
+            evs = tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
+            link_ev.append(evs)
+            e2e_step(i, evs)
         t1.record(s_out)
         torch.cuda.synchronize()
         barrier()
         e_ms = max_over_ranks(t0.elapsed_time(t1)) / args.steps
+        up_ms = sum(a.elapsed_time(b) for a, b, _, _ in link_ev)
+        down_ms = sum(c_.elapsed_time(d_) for _, _, c_, d_ in link_ev)
         # the same steps one after another on one stream (no overlap), for reference
         e2e_serial_step()
         torch.cuda.synchronize()
@@ -360,28 +392,47 @@ def run_gpu(args):
         e2e = dict(value=round(ws_n * flops_conv / (e_ms * 1e-3) / 1e12, 2), unit="TFLOPS", ms_per_step=round(e_ms, 3),
                    h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                    copies="pinned host buffers; uploads / backward / read-backs on three streams, double-buffered",
+                   h2d_gbs=round(h2d * args.steps / (up_ms * 1e-3) / 1e9, 1),
+                   d2h_gbs=round(d2h * args.steps / (down_ms * 1e-3) / 1e9, 1),
+                   link_note="GB/s = bytes over the copy streams' event time; the step is bound by the host link "
+                             "when (h2d + d2h bytes) / link GB/s exceeds the device step",
                    serial_ms_per_step=round(s_ms, 3),
                    serial_value=round(ws_n * flops_conv / (s_ms * 1e-3) / 1e12, 2))
         del pinned, host_out, dbufs, douts
 
     # accumulation variants at the headline size (p3's atomic_add / none comparison)
+    # accumulation variants: the group reduction of dK/dV ((a) in TMEM, (b) per-head CTAs adding into fp32)
+    # crossed with the way every fp32 partial is added (bulk tensor reduce, red.v4, scalar red, or plain
+    # stores -- wrong results, the cost floor), and the deterministic mode; [P3]'s atomic_add / none question
+    VARIANTS = (("tmem_bulk", dict(red_mode=nat.GQA_RED_BULK)),
+                ("tmem_v4", dict(red_mode=nat.GQA_RED_V4)),
+                ("tmem_scalar", dict(red_mode=nat.GQA_RED_SCALAR)),
+                ("tmem_none", dict(red_mode=nat.GQA_RED_NONE)),
+                ("atomic_bulk", dict(group_mode=nat.GQA_GROUP_ATOMIC, red_mode=nat.GQA_RED_BULK)),
+                ("atomic_v4", dict(group_mode=nat.GQA_GROUP_ATOMIC, red_mode=nat.GQA_RED_V4)),
+                ("atomic_none", dict(group_mode=nat.GQA_GROUP_ATOMIC, red_mode=nat.GQA_RED_NONE)),
+                ("deterministic", dict(deterministic=True)))
+
+    def run_variants(wv):
+        out = {}
+        nst = max(3, args.steps // 4)
+        for name, kw in VARIANTS:
+            cv = setup(wv, **kw)
+            ms, mms, _ = timed(cv, nst, args.warmup, main_events=True)
+            stp = ms / nst
+            out[name] = dict(tflops_exact=round(wv.flops_exact() / (stp * 1e-3) / 1e12, 2), ms=round(stp, 4),
+                             main_kernels_ms=round(mms, 4))
+            del cv
+        base = out["tmem_none"]["ms"]
+        out["overhead_vs_none"] = {n: round(out[n]["ms"] / base - 1.0, 4) for n in ("tmem_bulk", "tmem_v4", "tmem_scalar")}
+        out["overhead_vs_none"]["atomic_bulk_vs_atomic_none"] = round(out["atomic_bulk"]["ms"] / out["atomic_none"]["ms"] - 1.0, 4)
+        out["group_reduction_atomic_bulk_vs_tmem_bulk"] = round(out["atomic_bulk"]["ms"] / out["tmem_bulk"]["ms"] - 1.0, 4)
+        out["group_size"] = wv.Hq // wv.Hkv
+        return out
+
     variants = {}
     if not args.no_variants:
-        for name, kw in (("tmem_red_v4", dict(red_mode=nat.GQA_RED_V4)),
-                         ("tmem_red_none", dict(red_mode=nat.GQA_RED_NONE)),
-                         ("tmem_red_bulk", dict(red_mode=nat.GQA_RED_BULK)),
-                         ("tmem_red_scalar", dict(red_mode=nat.GQA_RED_SCALAR)),
-                         ("atomic_group_default_red", dict(group_mode=nat.GQA_GROUP_ATOMIC)),
-                         ("deterministic", dict(deterministic=True))):
-            cv = setup(w, **kw)
-            ms, mms, _ = timed(cv, max(3, args.steps // 2), args.warmup, main_events=True)
-            variants[name] = dict(tflops=round(flops_conv / (ms / max(3, args.steps // 2) * 1e-3) / 1e12, 2),
-                                  main_kernel_ms=round(mms, 4))
-            del cv
-        if "tmem_red_none" in variants:
-            for v_ in ("tmem_red_v4", "tmem_red_bulk"):
-                variants[f"overhead_{v_}_vs_none"] = round(
-                    variants["tmem_red_none"]["tflops"] / variants[v_]["tflops"] - 1.0, 4)
+        variants = run_variants(w)
 
     sweep = {}
     if not args.no_sweep:
@@ -395,7 +446,8 @@ def run_gpu(args):
                                      ws_.flops_exact() / (mms * 1e-3) / 1e12, 2))
             del cs
 
-    # the other workloads, same hot path and launch configuration (preprocess -> bwd -> postprocess [-> dsink])
+    # the other workloads, same hot path and launch configuration (preprocess -> bwd -> postprocess [-> dsink]);
+    # TFLOP/s on the exact, window-aware count first (the convention count ignores the window)
     configs = {}
     if not args.no_configs:
         for wc in (W.varlen(), W.sink_window(), W.long_context()):
@@ -403,11 +455,14 @@ def run_gpu(args):
             nst = max(3, args.steps // 2)
             ms, mms, _ = timed(cc, nst, args.warmup, main_events=True)
             stp = ms / nst
-            configs[wc.name] = dict(shape=wc.describe(), tflops=round(wc.flops_convention() / (stp * 1e-3) / 1e12, 2),
-                                    tflops_exact=round(wc.flops_exact() / (stp * 1e-3) / 1e12, 2), ms=round(stp, 4),
-                                    main_kernels_ms=round(mms, 4),
-                                    frac_of_peak_exact=round(wc.flops_exact() / (stp * 1e-3) / 1e12 / peaks["bf16_tflops"], 4))
+            te = wc.flops_exact() / (stp * 1e-3) / 1e12
+            configs[wc.name] = dict(tflops_exact=round(te, 2), frac_of_peak_exact=round(te / peaks["bf16_tflops"], 4),
+                                    ms=round(stp, 4), main_kernels_ms=round(mms, 4),
+                                    tflops_convention=round(wc.flops_convention() / (stp * 1e-3) / 1e12, 2),
+                                    shape=wc.describe())
             del cc
+            if not args.no_variants:
+                configs[wc.name]["variants"] = run_variants(wc)
 
     # the forward (prerequisite of the backward, not part of the step): exact-count TFLOP/s per workload
     forward = {}
@@ -434,6 +489,7 @@ def run_gpu(args):
                                     frac_of_peak_exact=round(fflops / (fms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4))
             if cf is not c:
                 del cf
+                drop(wf)
 
     # small, launch-bound problems: the eager chain of launches against one CUDA-graph replay of it
     graphs = {}
@@ -468,12 +524,10 @@ def run_gpu(args):
         line = dict(metric="GQA attention bwd TFLOPS (1xGB300, causal)", value=round(value, 2), unit="TFLOPS",
                     n_gpus=ws_n, steps=args.steps, warmup=args.warmup, ms_per_step=round(ms_step, 4),
                     higher_is_better=True, scaling="weak", vs_baseline=None, dtype="fp16", data="synthetic",
-                    config=dict(workload=w.name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, S=w.S, D=w.Dqk, causal=True,
-                                flop_count="2.5x forward, causal-halved", l2="inputs larger than L2, no flush",
-                                parallelism=f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
-                                mode="dK/dV summed in TMEM; dQ by " + (
-                                    "bulk tensor reduce" if pkg.preferred_red_mode(w.Dqk) == nat.GQA_RED_BULK
-                                    else "red.global.add.v4.f32")),
+                    config=_config(w.S, ws_n),
+                    mode="dK/dV summed in TMEM; dQ by " + (
+                        "bulk tensor reduce" if pkg.preferred_red_mode(w.Dqk) == nat.GQA_RED_BULK
+                        else "red.global.add.v4.f32"),
                     flops_per_step_convention=flops_conv, flops_per_step_exact=flops_exact,
                     frac_of_peak_exact=round(flops_exact / (ms_step * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
                     roofline=roofline, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clocks,
@@ -482,6 +536,13 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     ranks.close()
     return line
+
+
+def _config(n_ctx: int, ws_n: int) -> dict:
+    """The workload both arms report (the reference arm samples it, see its cpu_baseline)."""
+    return dict(workload=f"mha_causal_n{n_ctx}", B=4, Hq=8, Hkv=8, S=n_ctx, D=64, causal=True,
+                flop_count="2.5x forward, causal-halved", l2="inputs larger than L2, no flush",
+                parallelism=f"replicas x{ws_n}" if ws_n > 1 else "single GPU")
 
 
 def _oracle_sample(n: int):
@@ -531,8 +592,10 @@ def run_reference(args):
     ws_n, rank, _ = _dist()
     if rank != 0:
         return None
-    # each step a sample of about 0.4-1.5 s, less when many steps are asked for (the run stays near a minute)
-    n, w, timer, _ = _calibrated_sample(min(1.5, 60.0 / max(1, args.steps + args.warmup)))
+    # each step: the oracle backward of one of the workload's 32 (batch, head) pairs at the workload's own
+    # N_CTX (about 2 s on 16 Arm cores at 16384), so the line describes the same configuration
+    n = args.n_ctx
+    w, timer = _oracle_sample(n)
     for _ in range(args.warmup):
         timer()
     tot = sum(timer() for _ in range(args.steps))
@@ -541,8 +604,7 @@ def run_reference(args):
     line = dict(impl="reference", metric="GQA attention bwd TFLOPS (1xGB300, causal)", value=val, unit="TFLOPS",
                 n_gpus=ws_n, steps=args.steps, warmup=args.warmup, ms_per_step=round(1e3 * tot / args.steps, 3),
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                config=dict(workload=f"mha_causal_n{args.n_ctx}", B=4, Hq=8, Hkv=8, S=args.n_ctx, D=64,
-                            causal=True, flop_count="2.5x forward, causal-halved"),
+                config=_config(args.n_ctx, ws_n),
                 cpu_baseline=dict(kind="oracle", cores=cores, sample=_sample_text(n), value=val, unit="TFLOPS"),
                 e2e=dict(value=val, unit="TFLOPS", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)

@@ -32,6 +32,7 @@ EXPORTS = (
     "gqa_attn_workspace_size", "gqa_attn_fwd", "gqa_attn_bwd_preprocess", "gqa_attn_bwd",
     "gqa_attn_bwd_postprocess", "gqa_attn_dsink", "gqa_attn_get_device_error", "gqa_attn_set_wait_limit",
     "gqa_attn_selftest_wait_timeout", "gqa_attn_strerror", "gqa_attn_bwd_noalloc", "gqa_attn_params_size",
+    "gqa_attn_noalloc_get_device_error",
 )
 
 

@@ -426,3 +426,14 @@ extern "C" gqa_status gqa_attn_bwd_noalloc(const gqa_attn_params* p, const void*
   if ((s = gqa_attn_bwd(p, q, k, v, dout, dq, dk, dv, scratch, kNoAllocScratchBytes, stream)) != GQA_OK) return s;
   return gqa_attn_bwd_postprocess(p, dq, dk, dv, scratch, kNoAllocScratchBytes, stream);
 }
+
+// The error word of the scratch array: device-side failures of gqa_attn_bwd_noalloc (a packed
+// sequence longer than max_seqlen, malformed cu_seqlens, a wait that timed out) are recorded there,
+// and a caller without a workspace of its own reads them back through this call.
+extern "C" gqa_status gqa_attn_noalloc_get_device_error(void* stream, int* site) {
+  if (site) *site = 0;
+  void* scratch = nullptr;
+  gqa_status s = noalloc_scratch(&scratch);
+  if (s != GQA_OK) return s;
+  return gqa_attn_get_device_error(scratch, kNoAllocScratchBytes, stream, site);
+}

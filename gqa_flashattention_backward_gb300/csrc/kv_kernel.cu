@@ -406,7 +406,11 @@ __global__ void __launch_bounds__(448, 1)
         const int h = h_first + it / nt;
         const int t = t0 + it % nt;
         const int il = t * C::BQ + r;
-        if (!mbar_wait_warp(&ctl.dq_full, it & 1, guard, 19)) break;
+        bool got = mbar_wait_warp(&ctl.dq_full, it & 1, guard, 19);
+        // the transposing path meets at named barriers below: the four drain warps decide together
+        // whether to go on, so none leaves the loop while a sibling waits at a barrier for it
+        if (C::DQ_T) got = named_bar_and(2, 128, got);
+        if (!got) break;
         tc_fence_after();
         if (C::DQ_T) {
           // thread r = head-dim column r: the tile is transposed through shared memory

@@ -161,6 +161,18 @@ __device__ __forceinline__ void red_add_f32(float* p, float a) {
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Named barrier over `nthreads` threads that also ANDs `pred` across them: every participant gets
+// the same answer.  A group whose warps meet again at named barriers decides with it whether to go
+// on after a bounded wait, so no warp can leave while its siblings block at the next barrier.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 
 // ---------------------------------------------------------------- tcgen05 / TMEM
 // Allocation: executed by one full warp; the TMEM base address is written to *slot.
@@ -182,9 +194,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
-// CU_TENSOR_MAP_SWIZZLE_128B: 128-byte rows, 8-row / 1024-byte atoms, 16-byte
-// chunk index XOR row-in-atom). lbo/sbo in bytes.
 // Shared-memory matrix descriptor without swizzle: 8-row x 16-byte core matrices; for a K-major
 // operand `lbo` is the byte distance between core matrices adjacent along K and `sbo` between
 // core matrices adjacent along M / N (0 repeats one core matrix for every row group).
@@ -196,6 +205,9 @@ __device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uin
   d |= static_cast<uint64_t>(1) << 46;  // descriptor version for the tcgen05 path; swizzle mode 0
   return d;
 }
+// Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B: 128-byte rows, 8-row / 1024-byte atoms, 16-byte
+// chunk index XOR row-in-atom). lbo/sbo in bytes.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);

@@ -217,11 +217,20 @@ gqa_status gqa_attn_selftest_wait_timeout(void* workspace, size_t ws_bytes, void
  * address (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  All calls share the one array and it keeps the
  * last call's contents: calls that overlap on the GPU (other streams, other
- * threads) race and must be serialised by the caller.  Device-side errors are
- * recorded in the array and cannot be read back through gqa_attn_get_device_error. */
+ * threads) race and must be serialised by the caller.  Device-side errors (a
+ * packed sequence longer than max_seqlen, a wait that timed out) are recorded in
+ * the array's error word, which each call clears first: read them back with
+ * gqa_attn_noalloc_get_device_error. */
 gqa_status gqa_attn_bwd_noalloc(const gqa_attn_params* p, const void* q, const void* k, const void* v,
                                 const void* o, const void* dout, const float* lse, float* delta, void* dq,
                                 void* dk, void* dv, void* stream);
+
+/* Companion of gqa_attn_bwd_noalloc (no counterpart in the pages either): synchronises
+ * `stream`, then reports and clears the error word of the library's scratch array on the
+ * current device -- GQA_OK, GQA_ERR_DEVICE_TIMEOUT or GQA_ERR_DEVICE_INPUT, the raw word in
+ * *site if `site` is non-NULL -- as gqa_attn_get_device_error does for a caller workspace.
+ * Allocates nothing. */
+gqa_status gqa_attn_noalloc_get_device_error(void* stream, int* site);
 
 /* Human-readable name of a status. */
 const char* gqa_attn_strerror(gqa_status s);
