@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgqa_attn.so")
-SOURCES = ["api.cu", "elementwise.cu", "q_kernel.cu", "kv_kernel.cu"]
+SOURCES = ["api.cu", "elementwise.cu", "q_kernel.cu", "kv_kernel.cu", "fwd_kernel.cu"]
 HEADERS = ["common.cuh", "umma.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v", f"-I{os.path.join(ROOT, 'include')}"]

@@ -12,6 +12,7 @@
 #include "launch.h"
 
 namespace gqa {
+int fwd_kernel_bk(int Dqk);
 bool kv_kernel_has_dq(int Dqk);
 bool kv_kernel_has_bulk_dq(int Dqk);
 int kv_kernel_bq(int Dqk);
@@ -157,8 +158,10 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   pr.dq_st = resolve(p->dq_st, p->B, p->Hq, p->S, p->Dqk);
   pr.dk_st = resolve(p->dk_st, p->B, p->Hkv, pr.Sk, p->Dqk);
   pr.dv_st = resolve(p->dv_st, p->B, p->Hkv, pr.Sk, p->Dv);
+  // packed batches of up to kSchedMaxSeqs sequences: the main kernel takes them longest first
+  const bool use_sched = pr.cu_seqlens && pr.nseqs <= kSchedMaxSeqs;
   d.ws = ws_layout(pr.B, pr.Hq, pr.Hkv, pr.S, pr.Sk, pr.Dqk, pr.Dv, pr.nseqs, pr.ntiles, d.need_dq_acc,
-                   d.need_dkdv_acc, d.need_fold);
+                   d.need_dkdv_acc, d.need_fold, use_sched);
   uint8_t* base = static_cast<uint8_t*>(ws);
   pr.err = reinterpret_cast<int*>(base + d.ws.err_off);
   pr.nlse2 = reinterpret_cast<float*>(base + d.ws.lse2_off);
@@ -167,6 +170,7 @@ Derived derive(const gqa_attn_params* p, void* ws) {
   pr.dq_acc = d.need_dq_acc ? reinterpret_cast<float*>(base + d.ws.dq_off) : nullptr;
   pr.dk_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dk_off) : nullptr;
   pr.dv_acc = d.need_dkdv_acc ? reinterpret_cast<float*>(base + d.ws.dv_off) : nullptr;
+  pr.sched = (use_sched && base) ? reinterpret_cast<int*>(base + d.ws.sched_off) : nullptr;
   return d;
 }
 
@@ -232,7 +236,7 @@ gqa_status gqa_attn_fwd(const gqa_attn_params* p, const void* q, const void* k, 
   const bool bf = p->dtype == GQA_BF16;
   Maps m;
   std::memset(&m, 0, sizeof(m));
-  const int bk = q_kernel_bk();
+  const int bk = fwd_kernel_bk(p->Dqk);
   if (!map16(&m.q, q, p->Dqk, p->S, p->Hq, p->B, d.pr.q_st, 128, bf) || !map16(&m.k, k, p->Dqk, d.pr.Sk, p->Hkv, p->B, d.pr.k_st, bk, bf) ||
       !map16(&m.v, v, p->Dv, d.pr.Sk, p->Hkv, p->B, d.pr.v_st, bk, bf))
     return GQA_ERR_CUDA;

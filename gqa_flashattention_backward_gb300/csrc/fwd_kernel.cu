@@ -1,0 +1,422 @@
+// One-pass tcgen05 forward with causal / sliding-window / attention-sink masking
+// (tilelang-ascend PR #1638 "Add GQA Sink Backward BHSD", 4->2 commit:
+// "flashattn_fwd: online softmax + sink + window -> O, lse").
+//
+// One CTA owns two 128-row query tiles of one query head; softmax warpgroup w
+// (warps 4w..4w+3, thread r = query row r of tile w = TMEM lane r) keeps its own
+// running row maximum, row sum and O accumulator, so the two tiles need no
+// exchange and take turns on the tensor core: while warpgroup 0 exponentiates
+// its S of key tile j + 1, the tensor core computes warpgroup 1's P.V of tile j
+// and S of tile j + 1, and the other way round.  Per key tile of BK keys:
+//
+//   S_w  = Q_w . K^T                     (tcgen05, fp32 in TMEM)
+//   m    = running maximum of S_w * scale * log2(e) (sink included)
+//   P_w  = exp2(S_w * scale * log2(e) - m_ref), packed to 16 bits over S_w
+//   O_w += P_w . V                        (tcgen05, A operand from TMEM)
+//
+// m_ref, the maximum P is taken against, moves only when a row's maximum exceeds
+// it by more than TAU (log2 units), so P <= 2^TAU; then the warp rescales its O
+// rows in TMEM (and the row sums) by exp2(m_ref_old - m_ref_new) -- once S_w of
+// the tile is in TMEM every earlier MMA of the CTA has completed, P.V of the
+// previous tile included, and the next P.V waits for this warpgroup's P, so
+// nothing writes O meanwhile.  O = O_w / l and LSE = ln 2 * (m_ref + log2 l).
+//
+// Warp roles (320 threads): warps 0-3 / 4-7 the two softmax warpgroups, warp 8
+// the TMA producer (Q tiles once; K and V through rings of their own), warp 9
+// the TMEM allocator and MMA issuer (whole warp, one lane elected per MMA).
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <type_traits>
+#include "common.cuh"
+#include "umma.cuh"
+#include "launch.h"
+
+namespace gqa {
+
+template <int DQK, int DV, bool BF16>
+struct FwdCfg {
+  static constexpr int BQ = 128;                     // query rows per warpgroup tile = TMEM lanes
+  static constexpr int BK = (DQK <= 128) ? 128 : 64;  // keys per tile
+  static constexpr int Q_BYTES = BQ * DQK * 2;        // one query tile
+  static constexpr int K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
+  static constexpr int BUDGET = 225 * 1024;
+  // K stages first (S runs ahead of P.V), then V stages
+  static constexpr int VST = 2;
+  static constexpr int KST_RAW = (BUDGET - 2 * Q_BYTES - VST * V_BYTES) / K_BYTES;
+  static constexpr int KST = KST_RAW > 4 ? 4 : KST_RAW;
+  static constexpr int SMEM = 1024 + 2 * Q_BYTES + KST * K_BYTES + VST * V_BYTES;
+  // TMEM: per warpgroup S (BK columns, P packed over the first BK/2) then O (DV columns)
+  static constexpr uint32_t WG_COLS = BK + DV;
+  static constexpr uint32_t TMEM_COLS = 2 * WG_COLS <= 256 ? 256 : 512;
+  // P <= 2^TAU: fp16 exponentiates the fp16-rounded argument, whose rounding error grows with |x|,
+  // so it keeps the argument small; bf16 exponentiates in fp32
+  static constexpr float TAU = BF16 ? 8.f : 2.f;
+  static constexpr int THREADS = 320;
+  static_assert(KST >= 2, "key stages");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(2 * WG_COLS <= 512, "tmem");
+  static_assert(BK % 32 == 0 && DV % 64 == 0, "chunks");
+};
+
+struct FwdCtl {
+  uint64_t bar_q;
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[2], v_empty[2];
+  uint64_t s_full[2];   // tensor core -> warpgroup w: S_w of the next key tile is in TMEM
+  uint64_t p_full[2];   // warpgroup w -> tensor core: P_w stored (S_w read, O_w rescaled)
+  uint64_t acc_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int DQK, int DV, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    fwd_kernel(const Problem p, const __grid_constant__ Maps m, const float* __restrict__ sink, void* __restrict__ out,
+               float* __restrict__ lse_out) {
+  using C = FwdCfg<DQK, DV, BF16>;
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ FwdCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                          // tile w at sQ + w * Q_BYTES
+  uint8_t* sK0 = sQ + 2 * C::Q_BYTES;          // K stage st at sK0 + st * K_BYTES
+  uint8_t* sV0 = sK0 + C::KST * C::K_BYTES;    // V stage st at sV0 + st * V_BYTES
+
+  const int h = blockIdx.x;
+  const int s = blockIdx.z;
+  Seq sq, sk;
+  if (!load_seq(p, s, sq) || !load_kseq(p, s, sk)) return;
+  const int off = sk.len - sq.len;  // query i sits on key diagonal i + off
+  const int npair = (sq.len + 2 * C::BQ - 1) / (2 * C::BQ);
+  const int tp = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tile pairs first
+  if (tp >= npair) return;
+  // key tiles either query tile of the pair can see (a tile only one of them sees is masked for the other)
+  int k0, k1, ka, kb;
+  kv_tiles_for_q_tile(2 * tp, sq.len, sk.len, C::BK, p.right, p.window, &k0, &k1);
+  kv_tiles_for_q_tile(2 * tp + 1, sq.len, sk.len, C::BK, p.right, p.window, &ka, &kb);
+  if (2 * tp + 1 < (sq.len + C::BQ - 1) / C::BQ) {
+    if (ka < k0) k0 = ka;
+    if (kb > k1) k1 = kb;
+  }
+  if (k1 < k0) k1 = k0;
+  const int n = k1 - k0;
+  const int g = h / p.G;
+  const int zq = sq.b * p.Hq + h;
+
+  const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&ctl.bar_q, 1);
+    for (int i = 0; i < C::KST; ++i) {
+      mbar_init(&ctl.k_full[i], 1);
+      mbar_init(&ctl.k_empty[i], 1);
+    }
+    for (int i = 0; i < C::VST; ++i) {
+      mbar_init(&ctl.v_full[i], 1);
+      mbar_init(&ctl.v_empty[i], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&ctl.s_full[w], 1);
+      mbar_init(&ctl.p_full[w], 4);  // one arrival per warp of the warpgroup
+    }
+    mbar_init(&ctl.acc_done, 1);
+    ctl.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&ctl.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = __shfl_sync(0xffffffffu, ctl.tmem_base, 0);
+  const WaitGuard guard{p.err, &ctl.abort_flag, p.wait_limit};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&m.q);
+      tma_prefetch_map(&m.k);
+      tma_prefetch_map(&m.v);
+      mbar_expect_tx(&ctl.bar_q, 2 * C::Q_BYTES);
+      for (int w = 0; w < 2; ++w)
+        for (int cb = 0; cb < DQK / 64; ++cb)
+          tma_load_4d(sQ + w * C::Q_BYTES + cb * (C::BQ * 128), &m.q, &ctl.bar_q, cb * 64,
+                      sq.start + (2 * tp + w) * C::BQ, h, sq.b);
+      int issued_k = 0, issued_v = 0;
+      // K of tile i, then V of tile i - 1: the order the MMA warp consumes them
+      for (int i = 0; i <= n; ++i) {
+        if (i < n) {
+          const int st = i % C::KST;
+          if (i >= C::KST && !mbar_wait(&ctl.k_empty[st], ((i / C::KST) - 1) & 1, guard, 1)) break;
+          mbar_expect_tx(&ctl.k_full[st], C::K_BYTES);
+          for (int cb = 0; cb < DQK / 64; ++cb)
+            tma_load_4d(sK0 + st * C::K_BYTES + cb * (C::BK * 128), &m.k, &ctl.k_full[st], cb * 64,
+                        sk.start + (k0 + i) * C::BK, g, sk.b);
+          issued_k = i + 1;
+        }
+        const int vi = i - 1;
+        if (vi >= 0) {
+          const int vs = vi % C::VST;
+          if (vi >= C::VST && !mbar_wait(&ctl.v_empty[vs], ((vi / C::VST) - 1) & 1, guard, 1)) break;
+          mbar_expect_tx(&ctl.v_full[vs], C::V_BYTES);
+          for (int cb = 0; cb < DV / 64; ++cb)
+            tma_load_4d(sV0 + vs * C::V_BYTES + cb * (C::BK * 128), &m.v, &ctl.v_full[vs], cb * 64,
+                        sk.start + (k0 + vi) * C::BK, g, sk.b);
+          issued_v = vi + 1;
+        }
+      }
+      if (ctl.abort_flag) {
+        // let copies already in flight land before the CTA's shared memory goes away
+        volatile int no_abort = 0;
+        const WaitGuard g2{nullptr, &no_abort, p.wait_limit};
+        mbar_wait(&ctl.bar_q, 0, g2, 0);
+        for (int i = issued_k - C::KST < 0 ? 0 : issued_k - C::KST; i < issued_k; ++i)
+          mbar_wait(&ctl.k_full[i % C::KST], (i / C::KST) & 1, g2, 0);
+        for (int i = issued_v - C::VST < 0 ? 0 : issued_v - C::VST; i < issued_v; ++i)
+          mbar_wait(&ctl.v_full[i % C::VST], (i / C::VST) & 1, g2, 0);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idS = idesc_f16(128, C::BK, BF16, false, false);
+    constexpr uint32_t idPV = idesc_f16(128, DV, BF16, false, true);
+    const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);  // Q tile 0, K-major (A of S)
+    auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
+    bool ok = mbar_wait_warp(&ctl.bar_q, 0, guard, 2);
+    // S_w of key tile j into warpgroup w's S columns
+    auto issue_s = [&](int w, int j) {
+      const int st = j % C::KST;
+      const uint64_t dK = sdesc_sw128(smem_u32(sK0 + st * C::K_BYTES), 16, 1024);
+      const uint64_t dQ = desc_advance(dQ0, w * C::Q_BYTES);
+#pragma unroll 4
+      for (int kk = 0; kk < DQK / 16; ++kk)
+        umma_ss(tmem + w * C::WG_COLS, desc_advance(dQ, kstep(kk, C::BQ)), desc_advance(dK, kstep(kk, C::BK)), idS,
+                kk > 0);
+      umma_commit(&ctl.s_full[w]);
+    };
+    // O_w += P_w . V of key tile j (A = P packed over S_w, B = V read MN-major)
+    auto issue_pv = [&](int w, int j) {
+      const int vs = j % C::VST;
+      const uint64_t dVmn = sdesc_sw128(smem_u32(sV0 + vs * C::V_BYTES), C::BK * 128, 1024);
+      const uint32_t tS = tmem + w * C::WG_COLS;
+#pragma unroll
+      for (int kk = 0; kk < C::BK / 16; ++kk)
+        umma_ts(tS + C::BK, tS + kk * 8, desc_advance(dVmn, kk * 2048), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    if (ok && n > 0) {
+      ok = mbar_wait_warp(&ctl.k_full[0], 0, guard, 3);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        umma_commit(&ctl.k_empty[0]);
+      }
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const bool next = j + 1 < n;
+      const int kn = (j + 1) % C::KST;
+      if (!mbar_wait_warp(&ctl.v_full[j % C::VST], (j / C::VST) & 1, guard, 8)) break;
+      for (int w = 0; w < 2; ++w) {
+        // P_w of tile j in TMEM (S_w read): its P.V, then S_w of the next tile over the same columns
+        // (tcgen05.mma runs in issue order, so P.V has read P before S overwrites it)
+        if (!mbar_wait_warp(&ctl.p_full[w], j & 1, guard, 5)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(w, j);
+        if (next) {
+          if (w == 0 && !mbar_wait_warp(&ctl.k_full[kn], ((j + 1) / C::KST) & 1, guard, 3)) {
+            ok = false;
+            break;
+          }
+          issue_s(w, j + 1);
+        }
+      }
+      if (!ok) break;
+      umma_commit(&ctl.v_empty[j % C::VST]);
+      if (next) umma_commit(&ctl.k_empty[kn]);
+    }
+    umma_commit(&ctl.acc_done);
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int w = warp >> 2;
+    const int r = tid & 127;
+    const int il = (2 * tp + w) * C::BQ + r;  // query row within the sequence
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + w * C::WG_COLS, tO = tS + C::BK;
+    const float sl2 = p.scale_log2;
+    const float2 sl22 = make_float2(sl2, sl2);
+    const float sink2 = sink ? __ldg(sink + h) * kLog2e : -INFINITY;
+    // m_ref: the maximum P is taken against (-inf: nothing seen yet); l: row sum of P (the sink's term
+    // e^{sink - m_ref} included)
+    float mref = sink2;
+    float l = sink ? 1.f : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int j0 = (k0 + j) * C::BK;
+      const int i0 = (2 * tp + w) * C::BQ;
+      // some key of the tile past the sequence's end, right of the first row's reach or left of the last
+      // row's window (this covers tiles that only the other query tile of the pair sees)
+      const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && j0 + C::BK > i0 + off + p.right) ||
+                             (p.window > 0 && i0 + C::BQ - 1 + off - j0 >= p.window);
+      if (!mbar_wait_warp(&ctl.s_full[w], j & 1, guard, 6)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int d0 = il + off - j0;  // diagonal distance to this tile's first key
+      // P = exp2(S * scale * log2(e) - m_ref) of one 32-column chunk, masked, packed (16 words) and added
+      // into the row sums; returns the chunk's maximum of S * scale * log2(e)
+      float ls[4];
+      uint32_t pk[C::BK / 2];
+      auto chunk = [&](int c, float mu) -> float {
+        uint32_t v[32];
+        tmem_ld32(tS + 32 * c, v);
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!visible_d(d0 - 32 * c - e, j0 + 32 * c + e < sk.len, p.right, p.window)) v[e] = __float_as_uint(-INFINITY);
+        }
+        float c0 = -INFINITY, c1 = -INFINITY;
+        const float2 nm = make_float2(-mu, -mu);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float2 a = make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          const float2 b = make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          c0 = fmaxf(c0, fmaxf(a.x, a.y));
+          c1 = fmaxf(c1, fmaxf(b.x, b.y));
+          const float2 x0 = fma2(a, sl22, nm), x1 = fma2(b, sl22, nm);
+          if (BF16) {
+            const float p0 = ex2_approx(x0.x), p1 = ex2_approx(x0.y), p2 = ex2_approx(x1.x), p3 = ex2_approx(x1.y);
+            ls[0] += p0;
+            ls[1] += p1;
+            ls[2] += p2;
+            ls[3] += p3;
+            pk[16 * c + e / 2] = pack2<true>(p0, p1);
+            pk[16 * c + e / 2 + 1] = pack2<true>(p2, p3);
+          } else {
+            // the argument rounded to fp16, exponentiated two at a time
+            const uint32_t pa = ex2_f16x2(pack2<false>(x0.x, x0.y)), pb = ex2_f16x2(pack2<false>(x1.x, x1.y));
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
+            ls[0] += fa.x;
+            ls[1] += fa.y;
+            ls[2] += fb.x;
+            ls[3] += fb.y;
+            pk[16 * c + e / 2] = pa;
+            pk[16 * c + e / 2 + 1] = pb;
+          }
+        }
+        return fmaxf(c0, c1) * sl2;  // scale > 0 commutes with the maximum
+      };
+      // one pass against the current m_ref (the tile maximum found on the way); P never exceeds 2^TAU
+      float mu = (mref == -INFINITY) ? 0.f : mref;
+      float mt = -INFINITY;
+      ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
+#pragma unroll
+      for (int c = 0; c < C::BK / 32; ++c) mt = fmaxf(mt, chunk(c, mu));
+      // a row maximum above m_ref + TAU moves m_ref (the whole warp, as TMEM loads and stores are
+      // warp-collective): the O rows and the row sum are rescaled and the tile's P computed again
+      if (__any_sync(0xffffffffu, mt > mref + C::TAU)) {
+        const float mnew = fmaxf(mref, mt);
+        const float f = (mref == -INFINITY) ? 0.f : ex2_approx(mref - mnew);  // nothing accumulated yet: 0
+        l *= f;
+        if (j > 0) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < DV; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tO + c0, o);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st16(tO + c0, o);
+          }
+        }
+        mref = mnew;
+        mu = (mref == -INFINITY) ? 0.f : mref;
+        ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
+#pragma unroll
+        for (int c = 0; c < C::BK / 32; ++c) chunk(c, mu);  // (the maximum is known now)
+      }
+#pragma unroll
+      for (int c = 0; c < C::BK / 32; ++c) {
+        uint32_t q[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) q[e] = pk[16 * c + e];
+        tmem_st16(tS + 16 * c, q);
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&ctl.p_full[w]);
+    }
+    // epilogue: O = O_w / l, LSE = ln 2 * (m_ref + log2 l)
+    if (ok && mbar_wait_warp(&ctl.acc_done, 0, guard, 7)) {
+      tc_fence_after();
+      const bool valid = il < sq.len;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T* o = static_cast<T*>(out) + p.o_st.row(sq.b, h, sq.start + il);
+#pragma unroll 1
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t v[32];
+        if (n > 0) tmem_ld32(tO + c0, v);  // all lanes: .sync.aligned
+        else
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        if (valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 u;
+            u.x = pack2<BF16>(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+            u.y = pack2<BF16>(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+            u.z = pack2<BF16>(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+            u.w = pack2<BF16>(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
+            *reinterpret_cast<uint4*>(o + c0 + 8 * q4) = u;
+          }
+        }
+      }
+      if (valid) {
+        const float mu = (mref == -INFINITY) ? 0.f : mref;
+        lse_out[static_cast<size_t>(zq) * p.S + sq.start + il] = (l > 0.f) ? (mu + log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int DQK, int DV, bool BF16>
+static cudaError_t launch_fwd_t(const Problem& p, const Maps& m, const float* sink, void* out, float* lse,
+                                cudaStream_t st) {
+  using C = FwdCfg<DQK, DV, BF16>;
+  auto kern = fwd_kernel<DQK, DV, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int npair = (p.max_len + 2 * C::BQ - 1) / (2 * C::BQ);
+  if (npair == 0 || p.nseqs == 0) return cudaSuccess;
+  dim3 grid(p.Hq, npair, p.nseqs);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(p, m, sink, out, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const Problem& p, int dtype_bf16, const Maps& m, const float* sink, void* o, float* lse,
+                       cudaStream_t st) {
+#define GQA_F(DQK, DV)                                                               \
+  if (p.Dqk == DQK && p.Dv == DV)                                                    \
+    return dtype_bf16 ? launch_fwd_t<DQK, DV, true>(p, m, sink, o, lse, st)           \
+                      : launch_fwd_t<DQK, DV, false>(p, m, sink, o, lse, st);
+  GQA_F(64, 64)
+  GQA_F(128, 128)
+  GQA_F(192, 128)
+#undef GQA_F
+  return cudaErrorInvalidValue;
+}
+
+int fwd_kernel_bk(int Dqk) { return Dqk <= 128 ? 128 : 64; }
+
+}  // namespace gqa

@@ -568,11 +568,6 @@ static cudaError_t dispatch_q(const Problem& p, int bf16, const Maps& m, const f
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_fwd(const Problem& p, int dtype_bf16, const Maps& m, const float* sink, void* o, float* lse,
-                       cudaStream_t st) {
-  return dispatch_q<true>(p, dtype_bf16, m, sink, o, lse, st);
-}
-
 cudaError_t launch_dq(const Problem& p, int dtype_bf16, const Maps& m, void* dq, cudaStream_t st) {
   return dispatch_q<false>(p, dtype_bf16, m, nullptr, dq, nullptr, st);
 }
