@@ -55,6 +55,9 @@ struct Problem {
   int Sk;
   const int32_t* cu_seqlens_k;
   int max_len_k;
+  // packed batches: the main kernel's sequence order, longest first, written by the preprocess (null:
+  // the packing order)
+  int* sched;
 };
 
 // One sequence of the (possibly packed) batch.
@@ -122,6 +125,23 @@ __device__ __forceinline__ bool visible_d(int d, bool key_exists, int right, int
   return key_exists && (right <= 0 || d > -right) && (window <= 0 || d < window);
 }
 
+// ---------------------------------------------------------------- longest-first sequence order
+// The main kernel's grid runs sequence by sequence (each sequence's KV tiles together, so its query
+// tiles stay in L2 while they are read), tile 0 -- the heaviest under a causal mask -- first.  For
+// packed batches the preprocess writes the order of the sequences, longest (most KV tiles) first, so
+// short sequences fill the last wave instead of a long one arriving last: perm[slot] = sequence.
+constexpr int kSchedMaxSeqs = 256;  // sequences the one-block sort orders
+
+// perm[rank] = q for the sequences q < n ranked by key[q] (KV tiles), largest first, ties by index;
+// run by threads tid < nth of one block (or one host thread, nth = 1).
+__host__ __device__ inline void sched_fill(int* perm, const int* key, int n, int tid, int nth) {
+  for (int q = tid; q < n; q += nth) {
+    int rank = 0;
+    for (int t = 0; t < n; ++t) rank += (key[t] > key[q]) || (key[t] == key[q] && t < q);
+    perm[rank] = q;
+  }
+}
+
 // Index of the first float of a stats tile: head h, sequence s, 128-row tile t.
 __host__ __device__ __forceinline__ size_t stat_index(const Problem& p, int h, int s, int t) {
   return ((static_cast<size_t>(h) * p.nseqs + s) * p.ntiles + t) * kStatTile;
@@ -129,7 +149,7 @@ __host__ __device__ __forceinline__ size_t stat_index(const Problem& p, int h, i
 
 // ---------------------------------------------------------------- workspace
 struct WsLayout {
-  size_t err_off, lse2_off, delta_off, xf_off, dq_off, dk_off, dv_off, total;
+  size_t err_off, lse2_off, delta_off, xf_off, dq_off, dk_off, dv_off, sched_off, total;
 };
 
 constexpr int kFoldRowBytes = 32;  // 16 fp16 values per query row in an xfold tile
@@ -137,7 +157,7 @@ constexpr int kFoldRowBytes = 32;  // 16 fp16 values per query row in an xfold t
 __host__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 __host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Sk, int Dqk, int Dv, int nseqs, int ntiles,
-                                   bool need_dq_acc, bool need_dkdv_acc, bool need_fold) {
+                                   bool need_dq_acc, bool need_dkdv_acc, bool need_fold, bool need_sched = false) {
   WsLayout w{};
   size_t off = 0;
   w.err_off = off;
@@ -155,6 +175,8 @@ __host__ inline WsLayout ws_layout(int B, int Hq, int Hkv, int S, int Sk, int Dq
   if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * Sk * Dqk * 4);
   w.dv_off = off;
   if (need_dkdv_acc) off = align256(off + static_cast<size_t>(B) * Hkv * Sk * Dv * 4);
+  w.sched_off = off;
+  if (need_sched) off = align256(off + static_cast<size_t>(nseqs) * 4);
   w.total = off;
   return w;
 }

@@ -6,12 +6,14 @@
 //   postprocess : fp32 accumulators -> fp16/bf16 outputs (dual-output cast of the
 //                 same PR's 9->6 commit; the 4->2 commit's "fp32 atomic_add
 //                 then cast").
-//   dsink       : dsink_h = -sum_{b,i} exp(sink_h - lse) * Delta ("Kernel 9: Dsink").
+//   dsink       : dsink_h = -sum_{b,i} exp(sink_h - lse) * Delta ("Kernel 9: Dsink"), one
+//                 eight-CTA cluster per head.
 // All are grid-stride kernels sized to a multiple of the SM count with 16-byte
 // vector accesses.
+#include <cooperative_groups.h>
+#include <type_traits>
 #include "common.cuh"
 #include "umma.cuh"
-#include <type_traits>
 #include "launch.h"
 
 namespace gqa {
@@ -57,6 +59,21 @@ __device__ __forceinline__ void write_fold_row(uint8_t* tile, int q, float xl, f
   *reinterpret_cast<uint4*>(row + 128) = make_uint4(split_hi_lo(xd), 0u, 0u, 0u);
 }
 
+// The main kernel's sequence order (sched_fill), by one block from the packed key lengths.  A
+// malformed or over-long sequence counts 0 tiles (the main kernel reports it and skips it).
+__device__ void build_schedule(const Problem& p) {
+  __shared__ int key[kSchedMaxSeqs];
+  const int n = p.nseqs;
+  const int32_t* cu = p.cu_seqlens_k ? p.cu_seqlens_k : p.cu_seqlens;
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    const int a = __ldg(cu + q), e = __ldg(cu + q + 1);
+    const int len = e - a;
+    key[q] = (len < 0 || a < 0 || e > p.Sk || len > p.max_len_k) ? 0 : (len + 127) / 128;
+  }
+  __syncthreads();
+  sched_fill(p.sched, key, n, threadIdx.x, blockDim.x);
+}
+
 // 8 threads per row; each thread covers Dv/8 elements.
 template <typename T, int DV>
 __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __restrict__ o,
@@ -65,6 +82,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
   constexpr int PER = DV / 8;        // elements per thread
   constexpr int VEC = PER / 8;       // uint4 loads per thread per tensor
   const long long nrows = static_cast<long long>(p.B) * p.Hq * p.S;
+  if (p.sched && blockIdx.x == 0) build_schedule(p);
   const int sub = threadIdx.x & 7;
   const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 3);
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 3) + (threadIdx.x >> 3); r < nrows;
@@ -155,28 +173,46 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ acc
   }
 }
 
-// One block per head; fixed-order reduction (deterministic).
-__global__ void __launch_bounds__(512) dsink_kernel(int B, int Hq, int S, const float* __restrict__ sink,
-                                                    const float* __restrict__ lse,
-                                                    const float* __restrict__ delta, float* __restrict__ dsink) {
-  const int h = blockIdx.x;
+// One cluster of kDsinkCluster CTAs per head: CTA c of the cluster sums every kDsinkCluster-th block
+// of the head's B*S rows in a fixed order, then rank 0 adds the CTAs' sums in rank order through
+// distributed shared memory -- deterministic, and eight CTAs per head stream LSE / Delta instead of one.
+constexpr int kDsinkCluster = 8;
+constexpr int kDsinkThreads = 256;
+
+__global__ void __cluster_dims__(kDsinkCluster, 1, 1) __launch_bounds__(kDsinkThreads)
+    dsink_kernel(int B, int Hq, int S, const float* __restrict__ sink, const float* __restrict__ lse,
+                 const float* __restrict__ delta, float* __restrict__ dsink) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int h = blockIdx.x / kDsinkCluster;
+  const int c = static_cast<int>(cl.block_rank());
   const float sh = __ldg(sink + h);
+  const long long n = static_cast<long long>(B) * S;  // this head's rows over the batch
   float acc = 0.f;
-  for (int b = 0; b < B; ++b) {
-    const size_t base = (static_cast<size_t>(b) * Hq + h) * S;
-    for (int i = threadIdx.x; i < S; i += blockDim.x) acc += __expf(sh - __ldg(lse + base + i)) * __ldg(delta + base + i);
+  for (long long e = static_cast<long long>(c) * kDsinkThreads + threadIdx.x; e < n;
+       e += static_cast<long long>(kDsinkCluster) * kDsinkThreads) {
+    const long long b = e / S, i = e - b * S;
+    const size_t r = (static_cast<size_t>(b) * Hq + h) * S + i;
+    acc += __expf(sh - __ldg(lse + r)) * __ldg(delta + r);
   }
-  __shared__ float red[32];
+  __shared__ float red[kDsinkThreads / 32];
+  __shared__ float part;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (threadIdx.x == 0) dsink[h] = -v;
+  if (threadIdx.x == 0) {
+    float v = 0.f;
+    for (int wi = 0; wi < kDsinkThreads / 32; ++wi) v += red[wi];
+    part = v;
   }
+  cl.sync();  // every CTA's sum is in its shared memory
+  if (c == 0 && threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int k = 0; k < kDsinkCluster; ++k) tot += *cl.map_shared_rank(&part, k);
+    dsink[h] = -tot;
+  }
+  cl.sync();  // the peers keep their shared memory until rank 0 has read it
 }
 
 // Waits on a barrier that nothing completes: exercises the timeout path.
@@ -235,7 +271,8 @@ cudaError_t launch_cast(const float* acc, void* out, int B, int H, int S, int D,
 
 cudaError_t launch_dsink(int B, int Hq, int S, const float* sink, const float* lse, const float* delta,
                          float* dsink, cudaStream_t st) {
-  dsink_kernel<<<Hq, 512, 0, st>>>(B, Hq, S, sink, lse, delta, dsink);
+  if (Hq <= 0) return cudaSuccess;
+  dsink_kernel<<<Hq * kDsinkCluster, kDsinkThreads, 0, st>>>(B, Hq, S, sink, lse, delta, dsink);
   return cudaGetLastError();
 }
 

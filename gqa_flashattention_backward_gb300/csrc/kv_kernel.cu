@@ -48,7 +48,6 @@ struct KvCfg {
   // d=128: dQ^T = K^T . dS^T with the head dim on the 128 TMEM lanes (a 64-row query tile cannot
   // be the M of an MMA); the tile is transposed through shared memory for the reduction
   static constexpr bool DQ_T = (DQK == 128);
-  static constexpr bool DQ_ALIAS = false;                // dQ accumulator shares the dP/dS columns
   static constexpr bool HAS_STAGING = (DQK == 64);       // per-warp 32x32 staging for the bulk dQ reduce
   static constexpr int K_BYTES = BK * DQK * 2, V_BYTES = BK * DV * 2;
   static constexpr int Q_BYTES = BQ * DQK * 2, DO_BYTES = BQ * DV * 2;
@@ -75,7 +74,7 @@ struct KvCfg {
   static constexpr int SMEM = OFF_CTL + 256;
   // TMEM columns
   static constexpr uint32_t T_S = 0, T_DP = BQ, T_DV = 2 * BQ, T_DK = 2 * BQ + DV;
-  static constexpr uint32_t T_DQ = DQ_ALIAS ? T_DP : (T_DK + DQK);  // dQ (DQK cols) or dQ^T (BQ cols)
+  static constexpr uint32_t T_DQ = T_DK + DQK;  // dQ (DQK cols) or dQ^T (BQ cols)
   // packed dS^T (BQ/2 columns) in the 64 columns every head-dim configuration leaves free, so the
   // next tile's dP^T can be computed while dK still reads this tile's dS^T
   static constexpr uint32_t T_DSP = 448;
@@ -83,7 +82,7 @@ struct KvCfg {
   static constexpr int NCH = HALF / 32;                   // 32-column chunks per softmax warpgroup
   static constexpr int THREADS = 448;
   static_assert(SMEM <= 232448, "shared memory");
-  static_assert(T_DK + DQK <= T_DSP && (!HAS_DQ || DQ_ALIAS || T_DQ + (DQ_T ? BQ : DQK) <= T_DSP), "tmem");
+  static_assert(T_DK + DQK <= T_DSP && (!HAS_DQ || T_DQ + (DQ_T ? BQ : DQK) <= T_DSP), "tmem");
   static_assert(T_DSP + BQ / 2 <= 512, "tmem");
   // the dK/dV epilogue stages bulk reductions in the idle Q/dO stage buffers (8 warps x 8 KB)
   static_assert(ST * (Q_BYTES + DO_BYTES) >= 8 * 2 * 32 * 32 * 4, "epilogue staging");
@@ -183,12 +182,18 @@ __global__ void __launch_bounds__(448, 1)
   KvCtl& ctl = *reinterpret_cast<KvCtl*>(smem + C::OFF_CTL);
 
   const int head = blockIdx.x;   // kv head (group_tmem) or query head
-  const int s = blockIdx.z;
+  // y = KV tile (tile 0 has the most query tiles under a causal mask: launched first); z = sequence
+  // slot, mapped to a sequence by the longest-first order of packed batches
+  const int s = p.sched ? p.sched[blockIdx.z] : static_cast<int>(blockIdx.z);
+  if (static_cast<unsigned>(s) >= static_cast<unsigned>(p.nseqs)) {  // no preprocess on this workspace
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrBadSeqlens);
+    return;
+  }
   Seq sq, sk;  // the sequence's queries and keys
   if (!load_seq(p, s, sq) || !load_kseq(p, s, sk)) return;
   const int off = sk.len - sq.len;  // query i sits on key diagonal i + off
   const int ntk = (sk.len + C::BK - 1) / C::BK;
-  const int kt = blockIdx.y;     // tile 0 has the most query tiles under a causal mask: launched first
+  const int kt = blockIdx.y;
   if (kt >= ntk) return;
   if ((smem_u32(smem) & 1023u) != 0) {  // the operand layout needs a 1024-byte aligned base
     if (threadIdx.x == 0) atomicCAS(p.err, 0, 0x40000010);
@@ -339,8 +344,6 @@ __global__ void __launch_bounds__(448, 1)
       auto issue_dp = [&](int it) -> bool {
         const int st = it % C::ST;
         if (!mbar_wait_warp(&ctl.do_full[st], (it / C::ST) & 1, guard, 14)) return false;
-        // the dQ accumulator shares these columns: its drain must be finished
-        if (C::DQ_ALIAS && dq_on && it >= 1 && !mbar_wait_warp(&ctl.dq_empty, (it - 1) & 1, guard, 15)) return false;
         tc_fence_after();
         const uint64_t ddo = desc_advance(dDO_k0, st * C::DO_BYTES);
 #pragma unroll
@@ -373,9 +376,13 @@ __global__ void __launch_bounds__(448, 1)
           umma_ts(tmem + C::T_DK, tmem + C::T_DSP + kk * 8, desc_advance(dq_mn, kk * 2048), idDK,
                   (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&ctl.ds_free);
+        // the Q / dO stage is free once dK has read Q (S^T, dP^T and dV read it earlier): the producer
+        // loads the tile ST ahead while the dQ MMAs below, which read K and dS only, still run
+        umma_commit(&ctl.q_empty[st]);
         // dQ_partial = dS . K
         if (dq_on) {
-          if (!C::DQ_ALIAS && it >= 1 && !mbar_wait_warp(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
+          if (it >= 1 && !mbar_wait_warp(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
+          tc_fence_after();
           const uint32_t ds_off = (it & 1) * C::DS_BYTES;  // dS tiles alternate between two buffers
           if (C::DQ_T) {
             // dQ^T = K^T . dS^T : A = K tile read MN-major, B = dS read MN-major (query contiguous)
@@ -391,7 +398,6 @@ __global__ void __launch_bounds__(448, 1)
           umma_commit(&ctl.dq_full);
           umma_commit(&ctl.dsmem_free[it & 1]);
         }
-        umma_commit(&ctl.q_empty[st]);
       }
       umma_commit(&ctl.acc_done);
     }

@@ -19,6 +19,10 @@ def _cases():
         "mha": W.shrink(W.mha_causal(), name="mha_small", B=2, Hq=2, Hkv=2, S=520),
         "varlen": W.shrink(W.varlen(), name="varlen_small", Hq=8, Hkv=2, S=849,
                            varlen_lengths=[130, 1, 0, 257, 384, 77]),
+        # skewed packing: a long sequence first and late, short and empty ones between (the longest-first
+        # schedule of the main kernel reorders these items)
+        "varlen_skewed": W.shrink(W.varlen(), name="varlen_skewed", Hq=4, Hkv=1, S=9337,
+                                  varlen_lengths=[4096, 64, 64, 64, 3000, 1, 0, 2048]),
         "sink_window": W.shrink(W.sink_window(), name="sink_window_small", Hq=8, Hkv=1, S=600, window=200),
         "long_context": W.shrink(W.long_context(), name="long_context_small", Hq=4, Hkv=1, S=450),
         "noncausal64": W.Workload("noncausal64", 10, B=1, Hq=2, Hkv=1, S=300, Dqk=64, Dv=64,
