@@ -611,6 +611,68 @@ def run_reference(args):
     return line
 
 
+PROFILE_WORKLOADS = {
+    "tiny": lambda W: W.tiny(),
+    "mha_causal_n8192": lambda W: W.mha_causal(8192),
+    "mha_causal_n16384": lambda W: W.mha_causal(16384),
+    "varlen": lambda W: W.varlen(),
+    "sink_window": lambda W: W.sink_window(),
+    "long_context": lambda W: W.long_context(),
+}
+
+
+def run_only(args):
+    """One workload, one mode, nothing else: the command the ncu captures profile.  `--only NAME:MODE`
+    with MODE a backward variant (tmem_bulk (default), tmem_v4, tmem_scalar, tmem_none, atomic_bulk,
+    atomic_v4, atomic_none, deterministic) or "forward".  Runs `--warmup` + `--steps` steps and prints
+    the mean step time."""
+    import torch
+
+    import gqa_flashattention_backward_gb300 as pkg
+    from gqa_flashattention_backward_gb300 import _native as nat
+    from gqa_flashattention_backward_gb300 import workloads as W
+
+    name, _, mode = args.only.partition(":")
+    mode = mode or "tmem_bulk"
+    modes = dict(tmem_bulk=dict(red_mode=nat.GQA_RED_BULK), tmem_v4=dict(red_mode=nat.GQA_RED_V4),
+                 tmem_scalar=dict(red_mode=nat.GQA_RED_SCALAR), tmem_none=dict(red_mode=nat.GQA_RED_NONE),
+                 atomic_bulk=dict(group_mode=nat.GQA_GROUP_ATOMIC, red_mode=nat.GQA_RED_BULK),
+                 atomic_v4=dict(group_mode=nat.GQA_GROUP_ATOMIC, red_mode=nat.GQA_RED_V4),
+                 atomic_none=dict(group_mode=nat.GQA_GROUP_ATOMIC, red_mode=nat.GQA_RED_NONE),
+                 deterministic=dict(deterministic=True), forward=dict())
+    if name not in PROFILE_WORKLOADS or mode not in modes:
+        raise SystemExit(f"--only {args.only}: workload one of {sorted(PROFILE_WORKLOADS)}, mode one of {sorted(modes)}")
+    w = PROFILE_WORKLOADS[name](W)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    nat.load()
+    q, k, v, do, sink = (t.to(dev) if t is not None else None for t in W.make_inputs(w))
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev) if w.cu_seqlens else None
+    kw = dict(causal=w.causal, window=w.window, scale=w.resolved_scale, cu_seqlens=cu,
+              max_seqlen=w.max_seqlen if cu is not None else None)
+    o, lse = pkg.attention_forward(q, k, v, sink=sink, **kw)
+    ws = nat.alloc_workspace(pkg._params(q, k, v, w.causal, w.window, w.resolved_scale, cu, kw["max_seqlen"],
+                                         **modes[mode]), dev)
+    out = {}
+
+    def step():
+        if mode == "forward":
+            pkg.attention_forward(q, k, v, sink=sink, workspace=ws, **kw)
+        else:
+            pkg.attention_backward(q, k, v, o, lse, do, sink=sink, workspace=ws, out=out, **modes[mode], **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps(dict(only=args.only, ms_per_step=round(e0.elapsed_time(e1) / max(1, args.steps), 4))), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -625,10 +687,13 @@ def main():
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--no-forward", action="store_true", help="skip the forward timings")
     ap.add_argument("--no-graph", action="store_true", help="skip the eager / CUDA-graph comparison")
+    ap.add_argument("--only", default=None, help="WORKLOAD[:MODE]: one workload in one mode (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.only:
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

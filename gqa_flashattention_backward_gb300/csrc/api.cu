@@ -12,7 +12,6 @@
 #include "launch.h"
 
 namespace gqa {
-int fwd_kernel_bk(int Dqk);
 bool kv_kernel_has_dq(int Dqk);
 bool kv_kernel_has_bulk_dq(int Dqk);
 int kv_kernel_bq(int Dqk);

@@ -267,59 +267,93 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_after();
       const int d0 = il + off - j0;  // diagonal distance to this tile's first key
-      // P = exp2(S * scale * log2(e) - m_ref) of one 32-column chunk, masked, packed (16 words) and added
-      // into the row sums; returns the chunk's maximum of S * scale * log2(e)
-      float ls[4];
+      // P = exp2(S * scale * log2(e) - mu) of one 32-column chunk, masked, packed (16 words) and added into
+      // the row sums.  Returns the chunk's maximum -- bf16: of S * scale * log2(e), in fp32; fp16: of the
+      // exponent argument S * scale * log2(e) - mu as rounded to fp16 for the exponential (+inf past its range)
+      float2 lsum[2];
       uint32_t pk[C::BK / 2];
-      auto chunk = [&](int c, float mu) -> float {
-        uint32_t v[32];
+      auto load_chunk = [&](int c, uint32_t (&v)[32]) {
         tmem_ld32(tS + 32 * c, v);
         if (need_mask) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (!visible_d(d0 - 32 * c - e, j0 + 32 * c + e < sk.len, p.right, p.window)) v[e] = __float_as_uint(-INFINITY);
         }
-        float c0 = -INFINITY, c1 = -INFINITY;
-        const float2 nm = make_float2(-mu, -mu);
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float2 a = make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-          const float2 b = make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-          c0 = fmaxf(c0, fmaxf(a.x, a.y));
-          c1 = fmaxf(c1, fmaxf(b.x, b.y));
-          const float2 x0 = fma2(a, sl22, nm), x1 = fma2(b, sl22, nm);
-          if (BF16) {
-            const float p0 = ex2_approx(x0.x), p1 = ex2_approx(x0.y), p2 = ex2_approx(x1.x), p3 = ex2_approx(x1.y);
-            ls[0] += p0;
-            ls[1] += p1;
-            ls[2] += p2;
-            ls[3] += p3;
-            pk[16 * c + e / 2] = pack2<true>(p0, p1);
-            pk[16 * c + e / 2 + 1] = pack2<true>(p2, p3);
-          } else {
-            // the argument rounded to fp16, exponentiated two at a time
-            const uint32_t pa = ex2_f16x2(pack2<false>(x0.x, x0.y)), pb = ex2_f16x2(pack2<false>(x1.x, x1.y));
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
-            ls[0] += fa.x;
-            ls[1] += fa.y;
-            ls[2] += fb.x;
-            ls[3] += fb.y;
-            pk[16 * c + e / 2] = pa;
-            pk[16 * c + e / 2 + 1] = pb;
-          }
-        }
-        return fmaxf(c0, c1) * sl2;  // scale > 0 commutes with the maximum
       };
-      // one pass against the current m_ref (the tile maximum found on the way); P never exceeds 2^TAU
-      float mu = (mref == -INFINITY) ? 0.f : mref;
-      float mt = -INFINITY;
-      ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
+      auto chunk = [&](int c, float mu) -> float {
+        uint32_t v[32];
+        load_chunk(c, v);
+        const float2 nm = make_float2(-mu, -mu);
+        if constexpr (BF16) {
+          float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < C::BK / 32; ++c) mt = fmaxf(mt, chunk(c, mu));
-      // a row maximum above m_ref + TAU moves m_ref (the whole warp, as TMEM loads and stores are
-      // warp-collective): the O rows and the row sum are rescaled and the tile's P computed again
-      if (__any_sync(0xffffffffu, mt > mref + C::TAU)) {
+          for (int e = 0; e < 32; e += 4) {
+            const float2 a = make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            const float2 b = make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            c0 = fmaxf(c0, fmaxf(a.x, a.y));
+            c1 = fmaxf(c1, fmaxf(b.x, b.y));
+            const float2 x0 = fma2(a, sl22, nm), x1 = fma2(b, sl22, nm);
+            const float2 p01 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+            const float2 p23 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+            lsum[0] = add2(lsum[0], p01);
+            lsum[1] = add2(lsum[1], p23);
+            pk[16 * c + e / 2] = pack2<true>(p01.x, p01.y);
+            pk[16 * c + e / 2 + 1] = pack2<true>(p23.x, p23.y);
+          }
+          return fmaxf(c0, c1) * sl2;  // scale > 0 commutes with the maximum
+        } else {
+          // the argument rounded to fp16 and exponentiated two at a time; its maximum taken on the
+          // same packed pairs
+          __half2 hm = __halves2half2(__ushort_as_half(0xFC00u), __ushort_as_half(0xFC00u));  // -inf
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float2 x0 = fma2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sl22, nm);
+            const float2 x1 = fma2(make_float2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])), sl22, nm);
+            const uint32_t h0 = pack2<false>(x0.x, x0.y), h1 = pack2<false>(x1.x, x1.y);
+            hm = __hmax2(hm, __hmax2(*reinterpret_cast<const __half2*>(&h0), *reinterpret_cast<const __half2*>(&h1)));
+            pk[16 * c + e / 2] = ex2_f16x2(h0);
+            pk[16 * c + e / 2 + 1] = ex2_f16x2(h1);
+          }
+          // the chunk's 32 values of P (each <= 2^TAU) added in fp16: four partial sums of four pairs
+          // each, then combined (relative error below 3e-3 of the chunk sum), then into the fp32 row sum
+          const __half2* h = reinterpret_cast<const __half2*>(&pk[16 * c]);
+          const __half2 a = __hadd2(__hadd2(h[0], h[4]), __hadd2(h[8], h[12]));
+          const __half2 b = __hadd2(__hadd2(h[1], h[5]), __hadd2(h[9], h[13]));
+          const __half2 d = __hadd2(__hadd2(h[2], h[6]), __hadd2(h[10], h[14]));
+          const __half2 q = __hadd2(__hadd2(h[3], h[7]), __hadd2(h[11], h[15]));
+          lsum[c & 1] = add2(lsum[c & 1], __half22float2(__hadd2(__hadd2(a, b), __hadd2(d, q))));
+          const float2 fm = __half22float2(hm);
+          return fmaxf(fm.x, fm.y);
+        }
+      };
+      // one pass against the current m_ref; P never exceeds 2^TAU
+      float mu = (mref == -INFINITY) ? 0.f : mref;
+      float cm = -INFINITY;
+      lsum[0] = lsum[1] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < C::BK / 32; ++c) cm = fmaxf(cm, chunk(c, mu));
+      // a row maximum above m_ref + TAU (or the first finite one) moves m_ref (the whole warp, as TMEM loads
+      // and stores are warp-collective): the O rows and the row sum are rescaled and the tile's P computed again
+      const bool need = BF16 ? (cm > mref + C::TAU) : (mref == -INFINITY ? cm > -INFINITY : cm > C::TAU);
+      if (__any_sync(0xffffffffu, need)) {
+        // the tile maximum of S * scale * log2(e): bf16 has it in fp32; fp16 from its argument maximum (whose
+        // fp16 rounding leaves P <= 2^TAU up to a factor 1 + 2^-11 |x|), or -- when that overflowed -- again
+        // in fp32 from S
+        float mt = BF16 ? cm : cm + mu;
+        if (!BF16 && cm == INFINITY) {
+          float c0 = -INFINITY, c1 = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < C::BK / 32; ++c) {
+            uint32_t v[32];
+            load_chunk(c, v);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              c0 = fmaxf(c0, __uint_as_float(v[e]));
+              c1 = fmaxf(c1, __uint_as_float(v[e + 1]));
+            }
+          }
+          mt = fmaxf(c0, c1) * sl2;
+        }
         const float mnew = fmaxf(mref, mt);
         const float f = (mref == -INFINITY) ? 0.f : ex2_approx(mref - mnew);  // nothing accumulated yet: 0
         l *= f;
@@ -335,9 +369,9 @@ __global__ void __launch_bounds__(320, 1)
         }
         mref = mnew;
         mu = (mref == -INFINITY) ? 0.f : mref;
-        ls[0] = ls[1] = ls[2] = ls[3] = 0.f;
+        lsum[0] = lsum[1] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < C::BK / 32; ++c) chunk(c, mu);  // (the maximum is known now)
+        for (int c = 0; c < C::BK / 32; ++c) chunk(c, mu);
       }
 #pragma unroll
       for (int c = 0; c < C::BK / 32; ++c) {
@@ -346,7 +380,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int e = 0; e < 16; ++e) q[e] = pk[16 * c + e];
         tmem_st16(tS + 16 * c, q);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(&ctl.p_full[w]);

@@ -32,11 +32,12 @@ cudaError_t launch_dsink(int B, int Hq, int S, const float* sink, const float* l
                          float* dsink, cudaStream_t st);
 cudaError_t launch_selftest_wait(int* err, long long limit, cudaStream_t st);
 
-// Query-stationary kernels: forward (O, LSE) and the deterministic dQ pass.
+// One-pass forward (O, LSE); the K / V tensor-map box height (keys per tile) it needs.
 cudaError_t launch_fwd(const Problem& p, int dtype_bf16, const Maps& m, const float* sink, void* o, float* lse,
                        cudaStream_t st);
+int fwd_kernel_bk(int Dqk);
+// Query-stationary dQ pass (deterministic mode, head dim 192); keys per tile of it.
 cudaError_t launch_dq(const Problem& p, int dtype_bf16, const Maps& m, void* dq, cudaStream_t st);
-// Key rows per tile of the query-stationary kernels (the K / V tensor-map box height they need).
 int q_kernel_bk();
 
 // Key/value-stationary backward main kernel.
