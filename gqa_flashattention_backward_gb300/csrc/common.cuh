@@ -43,8 +43,8 @@ struct Problem {
   float* nlse2;       // [Hq][nseqs][ntiles][128]  -LSE * log2(e), -inf on padding rows
   float* ndelta;      // same layout, -Delta, 0 on padding rows (both negated so the
                       // kernels use one packed fma / add per pair of elements)
-  uint8_t* xfold;     // or null: [Hq][nseqs][ntiles] 4 KB tiles, one 32-byte fp16 row per query:
-                      // -LSE/scale and -Delta, each split hi + lo, in the tensor core's
+  uint8_t* xfold;     // or null: [Hq][nseqs][ntiles] 4 KB tiles, one 32-byte bf16 row per query:
+                      // -LSE/scale and -Delta, each split hi + mid + lo, in the tensor core's
                       // no-swizzle K-major layout (the main kernel adds them with an MMA)
   float* dq_acc;      // [B][Hq][S][Dqk] fp32
   float* dk_acc;      // [B][Hkv][S][Dqk] fp32
@@ -152,7 +152,7 @@ struct WsLayout {
   size_t err_off, lse2_off, delta_off, xf_off, dq_off, dk_off, dv_off, sched_off, total;
 };
 
-constexpr int kFoldRowBytes = 32;  // 16 fp16 values per query row in an xfold tile
+constexpr int kFoldRowBytes = 32;  // 16 bf16 values per query row in an xfold tile
 
 __host__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

@@ -42,21 +42,27 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int nseqs, int row) {
   return lo;
 }
 
-// One query row of an xfold tile: 16 fp16 values in the no-swizzle K-major core-matrix layout
+// One query row of an xfold tile: 16 bf16 values in the no-swizzle K-major core-matrix layout
 // (8 rows x 16 bytes per core matrix; the 8-row groups 256 bytes apart, the two K halves
-// 128 bytes apart).  K columns 0, 1 hold -LSE/scale as hi + lo; columns 8, 9 hold -Delta as
-// hi + lo; the rest are zero.  Adding this row through one K=16 MMA against a ones operand
-// subtracts LSE/scale from every logit of the row (resp. Delta from every dP) in fp32.
-__device__ __forceinline__ uint32_t split_hi_lo(float x) {
-  x = fminf(fmaxf(x, -60000.f), 60000.f);  // -inf (padding rows) -> a value that zeroes exp2
-  const __half hi = __float2half_rn(x);
-  const __half lo = __float2half_rn(x - __half2float(hi));
-  return static_cast<uint32_t>(__half_as_ushort(hi)) | (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
+// 128 bytes apart).  K columns 0-2 hold -LSE/scale as three bf16 terms hi + mid + lo, which add up
+// to the fp32 value exactly (each step's remainder has at most 16, then 8 significant bits) and
+// keep fp32's range; columns 8-10 hold -Delta the same way; the rest are zero.  Adding this row
+// through one K=16 MMA against a ones operand subtracts LSE/scale from every logit of the row
+// (resp. Delta from every dP) in fp32.
+__device__ __forceinline__ uint2 split3(float x) {
+  x = fminf(fmaxf(x, -1e30f), 1e30f);  // -inf (padding rows) -> a value that zeroes exp2
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r - __bfloat162float(mid));
+  return make_uint2(static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16),
+                    static_cast<uint32_t>(__bfloat16_as_ushort(lo)));
 }
 __device__ __forceinline__ void write_fold_row(uint8_t* tile, int q, float xl, float xd) {
   uint8_t* row = tile + (q >> 3) * 256 + (q & 7) * 16;
-  *reinterpret_cast<uint4*>(row) = make_uint4(split_hi_lo(xl), 0u, 0u, 0u);
-  *reinterpret_cast<uint4*>(row + 128) = make_uint4(split_hi_lo(xd), 0u, 0u, 0u);
+  const uint2 l = split3(xl), d = split3(xd);
+  *reinterpret_cast<uint4*>(row) = make_uint4(l.x, l.y, 0u, 0u);
+  *reinterpret_cast<uint4*>(row + 128) = make_uint4(d.x, d.y, 0u, 0u);
 }
 
 // The main kernel's sequence order (sched_fill), by one block from the packed key lengths.  A

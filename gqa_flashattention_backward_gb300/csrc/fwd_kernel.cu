@@ -337,10 +337,10 @@ __global__ void __launch_bounds__(320, 1)
       const bool need = BF16 ? (cm > mref + C::TAU) : (mref == -INFINITY ? cm > -INFINITY : cm > C::TAU);
       if (__any_sync(0xffffffffu, need)) {
         // the tile maximum of S * scale * log2(e): bf16 has it in fp32; fp16 from its argument maximum (whose
-        // fp16 rounding leaves P <= 2^TAU up to a factor 1 + 2^-11 |x|), or -- when that overflowed -- again
-        // in fp32 from S
+        // fp16 rounding leaves P <= 2^TAU up to a factor 1 + 2^-11 |x|), or -- when that overflowed in any
+        // row of the warp -- again in fp32 from S, by the whole warp (the TMEM loads are warp-collective)
         float mt = BF16 ? cm : cm + mu;
-        if (!BF16 && cm == INFINITY) {
+        if (!BF16 && __any_sync(0xffffffffu, cm == INFINITY)) {
           float c0 = -INFINITY, c1 = -INFINITY;
 #pragma unroll 1
           for (int c = 0; c < C::BK / 32; ++c) {

@@ -54,7 +54,8 @@ struct KvCfg {
   static constexpr int ST = 3;
   static constexpr int DS_BYTES = HAS_DQ ? BQ * BK * 2 : 0;   // one dS tile; two alternate
   // head dim 64: -LSE/scale and -Delta enter Sᵀ and dPᵀ through one extra K=16 MMA each (an xfold
-  // tile per stage against constant ones operands) instead of per-element shared-memory loads
+  // tile of bf16 hi + mid + lo terms per stage against constant ones operands) instead of
+  // per-element shared-memory loads
   static constexpr bool FOLD = (DQK == 64);
   static constexpr int X_BYTES = FOLD ? BQ * kFoldRowBytes : 0;
   static constexpr int STAT_BYTES = FOLD ? 0 : BQ * 4;          // LSE / Delta vector per stage
@@ -237,9 +238,9 @@ __global__ void __launch_bounds__(448, 1)
     tmem_relinquish();
   }
   if (C::FOLD && tid < C::ONES_BYTES / 16) {
-    // fp16 core matrices ones | zeros | ones: the A operands that add the xfold columns 0-7
+    // bf16 core matrices ones | zeros | ones: the A operands that add the xfold columns 0-7
     // (start 0) or 8-15 (start 128) of each query row to every logit of that row
-    const uint32_t v = (tid / 8 == 1) ? 0u : 0x3C003C00u;
+    const uint32_t v = (tid / 8 == 1) ? 0u : 0x3F803F80u;
     reinterpret_cast<uint4*>(smem + C::OFF_ONES)[tid] = make_uint4(v, v, v, v);
     fence_async_smem();
   }
@@ -321,8 +322,8 @@ __global__ void __launch_bounds__(448, 1)
       const uint64_t dQ_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), C::BQ * 128, 1024);
       const uint64_t dDO_k0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
       const uint64_t dDO_mn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), C::BQ * 128, 1024);
-      // the fold: ones (A, fp16, no swizzle, one core matrix pair for every row group) x xfold tile (B)
-      constexpr uint32_t idF = idesc_f16(128, C::BQ, false, false, false);
+      // the fold: ones (A, bf16, no swizzle, one core matrix pair for every row group) x xfold tile (B, bf16)
+      constexpr uint32_t idF = idesc_f16(128, C::BQ, true, false, false);
       const uint64_t dAL = sdesc_none(smem_u32(smem + C::OFF_ONES), 128, 0);        // K columns 0-7
       const uint64_t dAD = sdesc_none(smem_u32(smem + C::OFF_ONES) + 128, 128, 0);  // K columns 8-15
       const uint64_t dX0 = sdesc_none(smem_u32(smem + C::OFF_X), 128, 256);
