@@ -79,12 +79,19 @@ struct KvCfg {
   // packed dS^T (BQ/2 columns) in the 64 columns every head-dim configuration leaves free, so the
   // next tile's dP^T can be computed while dK still reads this tile's dS^T
   static constexpr uint32_t T_DSP = 448;
+  // head dim 64: the stationary K and V tiles are also copied into TMEM (the last 64 columns, packed
+  // 16-bit like P), so S^T = K . Q^T and dP^T = V . dO^T take their A operand from TMEM instead of
+  // shared memory (32 KB less shared-memory traffic per tile); packed dS^T then goes over dP^T, like
+  // P^T over S^T, and the next tile's dP^T follows this tile's dK
+  static constexpr bool KV_TMEM = (DQK == 64 && DV == 64);
+  static constexpr uint32_t T_K = 448, T_V = 480;
   static constexpr int HALF = BQ / 2;                   // query columns per softmax warpgroup
   static constexpr int NCH = HALF / 32;                   // 32-column chunks per softmax warpgroup
   static constexpr int THREADS = 448;
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(T_DK + DQK <= T_DSP && (!HAS_DQ || T_DQ + (DQ_T ? BQ : DQK) <= T_DSP), "tmem");
   static_assert(T_DSP + BQ / 2 <= 512, "tmem");
+  static_assert(!KV_TMEM || (T_DQ + DQK <= T_K && T_V + DV / 2 <= 512 && BQ == 128), "tmem: K and V");
   // the dK/dV epilogue stages bulk reductions in the idle Q/dO stage buffers (8 warps x 8 KB)
   static_assert(ST * (Q_BYTES + DO_BYTES) >= 8 * 2 * 32 * 32 * 4, "epilogue staging");
 };
@@ -94,6 +101,7 @@ struct KvCtl {
   uint64_t q_full[3], do_full[3], q_empty[3];
   uint64_t s_full, dp_full, p_full, ds_full, ds_free;
   uint64_t dq_full, dq_empty, dsmem_free[2], acc_done;
+  uint64_t kv_tmem;  // K and V copied into TMEM (head dim 64)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -230,6 +238,7 @@ __global__ void __launch_bounds__(448, 1)
     mbar_init(&ctl.dsmem_free[0], 1);
     mbar_init(&ctl.dsmem_free[1], 1);
     mbar_init(&ctl.acc_done, 1);
+    mbar_init(&ctl.kv_tmem, 8);  // one arrival per softmax warp
     ctl.abort_flag = 0;
     fence_mbar_init();
   }
@@ -330,14 +339,19 @@ __global__ void __launch_bounds__(448, 1)
       // K-major operand with 64-element (128-byte) rows: K step kk lives in 64-column block kk/4 at byte kk%4*32
       auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
       bool ok = mbar_wait_warp(&ctl.kv_full, 0, guard, 12);
+      if (C::KV_TMEM && ok && NIT > 0) ok = mbar_wait_warp(&ctl.kv_tmem, 0, guard, 26);
       auto issue_s = [&](int it) -> bool {
         const int st = it % C::ST;
         if (!mbar_wait_warp(&ctl.q_full[st], (it / C::ST) & 1, guard, 13)) return false;
         tc_fence_after();
         const uint64_t dq = desc_advance(dQ_k0, st * C::Q_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk)
-          umma_ss(tmem + C::T_S, desc_advance(dK_k, kstep(kk, C::BK)), desc_advance(dq, kstep(kk, C::BQ)), idS, kk > 0);
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          if constexpr (C::KV_TMEM)
+            umma_ts(tmem + C::T_S, tmem + C::T_K + kk * 8, desc_advance(dq, kstep(kk, C::BQ)), idS, kk > 0);
+          else
+            umma_ss(tmem + C::T_S, desc_advance(dK_k, kstep(kk, C::BK)), desc_advance(dq, kstep(kk, C::BQ)), idS, kk > 0);
+        }
         if (C::FOLD) umma_ss(tmem + C::T_S, dAL, desc_advance(dX0, st * C::X_BYTES), idF, 1u);  // - LSE/scale
         umma_commit(&ctl.s_full);
         return true;
@@ -348,8 +362,12 @@ __global__ void __launch_bounds__(448, 1)
         tc_fence_after();
         const uint64_t ddo = desc_advance(dDO_k0, st * C::DO_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk)
-          umma_ss(tmem + C::T_DP, desc_advance(dV_k, kstep(kk, C::BK)), desc_advance(ddo, kstep(kk, C::BQ)), idS, kk > 0);
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          if constexpr (C::KV_TMEM)
+            umma_ts(tmem + C::T_DP, tmem + C::T_V + kk * 8, desc_advance(ddo, kstep(kk, C::BQ)), idS, kk > 0);
+          else
+            umma_ss(tmem + C::T_DP, desc_advance(dV_k, kstep(kk, C::BK)), desc_advance(ddo, kstep(kk, C::BQ)), idS, kk > 0);
+        }
         if (C::FOLD) umma_ss(tmem + C::T_DP, dAD, desc_advance(dX0, st * C::X_BYTES), idF, 1u);  // - Delta
         umma_commit(&ctl.dp_full);
         return true;
@@ -368,18 +386,31 @@ __global__ void __launch_bounds__(448, 1)
                   (it > 0 || kk > 0) ? 1u : 0u);
         // next tile's S^T (its columns were read by the softmax warps, P^T was consumed by the dV MMA above)
         if (it + 1 < NIT && !issue_s(it + 1)) break;
-        // the softmax warps are idle until the next tile's dP^T: it goes first, then dK += dS^T . Q
         if (!mbar_wait_warp(&ctl.ds_full, it & 1, guard, 17)) break;
-        if (it + 1 < NIT && !issue_dp(it + 1)) break;
-        tc_fence_after();
+        if constexpr (C::KV_TMEM) {
+          // dK += dS^T . Q with dS^T packed over dP^T, then the next tile's dP^T over the same columns
+          // (tcgen05.mma runs in issue order, so dK has read dS^T before dP^T overwrites it)
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)
-          umma_ts(tmem + C::T_DK, tmem + C::T_DSP + kk * 8, desc_advance(dq_mn, kk * 2048), idDK,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&ctl.ds_free);
-        // the Q / dO stage is free once dK has read Q (S^T, dP^T and dV read it earlier): the producer
-        // loads the tile ST ahead while the dQ MMAs below, which read K and dS only, still run
-        umma_commit(&ctl.q_empty[st]);
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_advance(dq_mn, kk * 2048), idDK,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&ctl.ds_free);
+          umma_commit(&ctl.q_empty[st]);
+          if (it + 1 < NIT && !issue_dp(it + 1)) break;
+        } else {
+          // the softmax warps are idle until the next tile's dP^T: it goes first, then dK += dS^T . Q
+          if (it + 1 < NIT && !issue_dp(it + 1)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            umma_ts(tmem + C::T_DK, tmem + C::T_DSP + kk * 8, desc_advance(dq_mn, kk * 2048), idDK,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&ctl.ds_free);
+          // the Q / dO stage is free once dK has read Q (S^T, dP^T and dV read it earlier): the producer
+          // loads the tile ST ahead while the dQ MMAs below, which read K and dS only, still run
+          umma_commit(&ctl.q_empty[st]);
+        }
         // dQ_partial = dS . K
         if (dq_on) {
           if (it >= 1 && !mbar_wait_warp(&ctl.dq_empty, (it - 1) & 1, guard, 18)) break;
@@ -514,6 +545,33 @@ __global__ void __launch_bounds__(448, 1)
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     const bool dq_on = C::HAS_DQ && dq_mode != kDqNone;
     bool ok = true;
+    if constexpr (C::KV_TMEM) {
+      // warpgroup 0 copies K, warpgroup 1 V into TMEM: thread r moves key row r (128 bytes, 128-byte
+      // swizzled in shared memory: 16-byte chunk c of row r sits at chunk c ^ (r % 8)) into 32 packed
+      // columns of lane r
+      if (NIT > 0) {
+        if (!mbar_wait_warp(&ctl.kv_full, 0, guard, 27)) {
+          ok = false;
+        } else {
+          const uint8_t* row = smem + (wg == 0 ? C::OFF_K : C::OFF_V) + r * 128;
+          uint32_t w[2][16];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) * 16));
+            w[c / 4][(c % 4) * 4 + 0] = u.x;
+            w[c / 4][(c % 4) * 4 + 1] = u.y;
+            w[c / 4][(c % 4) * 4 + 2] = u.z;
+            w[c / 4][(c % 4) * 4 + 3] = u.w;
+          }
+          const uint32_t tkv = tmem + lane_base + (wg == 0 ? C::T_K : C::T_V);
+          tmem_st16(tkv, w[0]);
+          tmem_st16(tkv + 16, w[1]);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive_warp(&ctl.kv_tmem);
+        }
+      }
+    }
     for (int it = 0; ok && it < NIT; ++it) {
       const int st = it % C::ST;
       const int t = t0 + it % nt;
@@ -544,11 +602,7 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_after();
       // P^T = exp2(S^T * scale*log2e - LSE2) for this warpgroup's columns, kept packed (16-bit) for dS
       uint32_t pk[C::HALF / 2];
-      uint32_t vs[C::HALF];
-      tmem_ld_half<C::HALF>(tmem + lane_base + C::T_S + cbase, vs);
-#pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        const uint32_t* v = vs + 32 * c;
+      auto p_chunk = [&](int c, const uint32_t (&v)[32]) {
         if (BF16) {
           float pf[32];
 #pragma unroll
@@ -583,6 +637,20 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) pc[e] = pk[16 * c + e];
         tmem_st16(tmem + lane_base + C::T_S + cbase + 16 * c, pc);
+      };
+      // 32-column chunks: the second one's load runs while the first is exponentiated
+      {
+        uint32_t va[32];
+        tmem_ld32(tmem + lane_base + C::T_S + cbase, va);
+        if constexpr (C::NCH == 2) {
+          uint32_t vb[32];
+          tmem_ld32_start(tmem + lane_base + C::T_S + cbase + 32, vb);
+          p_chunk(0, va);
+          tmem_ld_wait(vb);
+          p_chunk(1, vb);
+        } else {
+          p_chunk(0, va);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -602,10 +670,7 @@ __global__ void __launch_bounds__(448, 1)
         break;
       }
       tc_fence_after();
-      tmem_ld_half<C::HALF>(tmem + lane_base + C::T_DP + cbase, vs);
-#pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        const uint32_t* v = vs + 32 * c;
+      auto ds_chunk = [&](int c, const uint32_t (&v)[32]) {
         uint32_t ds[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
@@ -619,7 +684,7 @@ __global__ void __launch_bounds__(448, 1)
           ds[2 * q4] = mul_packed<BF16>(pk[16 * c + 2 * q4], pack2<BF16>(a.x, a.y));
           ds[2 * q4 + 1] = mul_packed<BF16>(pk[16 * c + 2 * q4 + 1], pack2<BF16>(b.x, b.y));
         }
-        tmem_st16(tmem + lane_base + C::T_DSP + cbase / 2 + 16 * c, ds);
+        tmem_st16(tmem + lane_base + (C::KV_TMEM ? C::T_DP + cbase : C::T_DSP + cbase / 2) + 16 * c, ds);
         if (dq_on) {
           // dS for the dQ MMA: MN-major (query index contiguous), 128B swizzle, key row r = K index
           const int c0 = cbase + 32 * c;
@@ -629,6 +694,21 @@ __global__ void __launch_bounds__(448, 1)
             const int chunk = ((c0 % 64) / 8 + q) ^ (r & 7);
             *reinterpret_cast<uint4*>(sds + chunk * 16) = make_uint4(ds[4 * q], ds[4 * q + 1], ds[4 * q + 2], ds[4 * q + 3]);
           }
+        }
+      };
+      {
+        uint32_t va[32];
+        tmem_ld32(tmem + lane_base + C::T_DP + cbase, va);
+        if constexpr (C::NCH == 2) {
+          // the second chunk's dP^T is read before the first chunk's dS^T is stored over dP^T's columns
+          // 0-15 of this warpgroup (and it never overlaps them: its columns are 32-63)
+          uint32_t vb[32];
+          tmem_ld32_start(tmem + lane_base + C::T_DP + cbase + 32, vb);
+          ds_chunk(0, va);
+          tmem_ld_wait(vb);
+          ds_chunk(1, vb);
+        } else {
+          ds_chunk(0, va);
         }
       }
       tmem_st_wait();
