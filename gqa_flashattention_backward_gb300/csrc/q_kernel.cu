@@ -43,11 +43,18 @@ struct QCfg {
   static constexpr int NBUF = 2;
   static constexpr uint32_t BUF = 2 * BK;
   static constexpr uint32_t T_ACC = NBUF * BUF;
-  static constexpr uint32_t TMEM_COLS = (T_ACC + DQK <= 256) ? 256 : 512;
+  // the stationary dO and Q tiles as TMEM A operands (packed 16-bit pairs, like P), after the
+  // accumulator: dO always, Q where the 512 columns allow (head dims 64 and 128).  The N = 64 S and dP
+  // MMAs then read only their B operand (the key tile) from shared memory: with both operands there
+  // they need 6 KB per 32 cycles of math, more than shared memory's 128 bytes per cycle
+  static constexpr uint32_t T_DO = T_ACC + DQK;
+  static constexpr uint32_t T_Q = T_DO + DV / 2;
+  static constexpr bool Q_TMEM = T_Q + DQK / 2 <= 512;
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int THREADS = 320;
   static_assert(KST >= 2, "stages");
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(T_ACC + DQK <= 512, "tmem");
+  static_assert(T_DO + DV / 2 <= 512, "tmem");
   static_assert(DQK % 64 == 0, "each warpgroup drains whole 32-column chunks");
 };
 
@@ -57,6 +64,7 @@ struct QSmemCtl {
   uint64_t s_full[2];   // tensor core -> warpgroup: S and dP of the buffer's tile are in TMEM
   uint64_t sm_done[2];  // warpgroup -> tensor core: dS stored, buffer reusable
   uint64_t acc_done;
+  uint64_t op_tmem;     // softmax warps -> tensor core: dO (and Q) copied into TMEM
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -101,6 +109,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&ctl.sm_done[i], 4);  // one arrival per warp of the warpgroup
     }
     mbar_init(&ctl.acc_done, 1);
+    mbar_init(&ctl.op_tmem, 8);  // one arrival per softmax warp
     ctl.abort_flag = 0;
     fence_mbar_init();
   }
@@ -154,9 +163,9 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idS = idesc_f16(128, C::BK, BF16, false, false);
       constexpr uint32_t idDQ = idesc_f16(128, DQK, BF16, false, true);
       const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);    // Q, K-major (A of S)
-      const uint64_t dDO0 = sdesc_sw128(smem_u32(sDO), 16, 1024);  // dO, K-major (A of dP)
       auto kstep = [](int kk, int rows) -> uint32_t { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
       bool ok = mbar_wait_warp(&ctl.bar_q, 0, guard, 2);
+      if (ok && NIT > 0) ok = mbar_wait_warp(&ctl.op_tmem, 0, guard, 9);
       // S and dP of tile `it` into buffer it % 2, once the tile two earlier has left it
       auto issue_s = [&](int it) -> bool {
         const int st = it % C::KST, b = it % C::NBUF;
@@ -169,11 +178,15 @@ __global__ void __launch_bounds__(320, 1)
         const uint64_t dV = sdesc_sw128(aK + C::K_BYTES, 16, 1024);
         const uint32_t tS = tmem + b * C::BUF;
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk)
-          umma_ss(tS, desc_advance(dQ0, kstep(kk, C::BQ)), desc_advance(dK, kstep(kk, C::BK)), idS, kk > 0);
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          if constexpr (C::Q_TMEM)
+            umma_ts(tS, tmem + C::T_Q + kk * 8, desc_advance(dK, kstep(kk, C::BK)), idS, kk > 0);
+          else
+            umma_ss(tS, desc_advance(dQ0, kstep(kk, C::BQ)), desc_advance(dK, kstep(kk, C::BK)), idS, kk > 0);
+        }
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
-          umma_ss(tS + C::BK, desc_advance(dDO0, kstep(kk, C::BQ)), desc_advance(dV, kstep(kk, C::BK)), idS, kk > 0);
+          umma_ts(tS + C::BK, tmem + C::T_DO + kk * 8, desc_advance(dV, kstep(kk, C::BK)), idS, kk > 0);
         umma_commit(&ctl.s_full[b]);
         return true;
       };
@@ -210,7 +223,39 @@ __global__ void __launch_bounds__(320, 1)
     const size_t sidx = stat_index(p, h, s, t) + r;
     const float nlse2 = p.nlse2[sidx];
     const float ndlt = p.ndelta[sidx];
-    for (int it = w; it < NIT; it += 2) {
+    // warpgroup 0 copies dO, warpgroup 1 Q (where it goes to TMEM) into TMEM: thread r moves row r,
+    // 128 bytes per 64-column block (128-byte swizzled in shared memory: 16-byte chunk c of row r sits
+    // at chunk c ^ (r % 8)) into 32 packed columns of lane r
+    if (NIT > 0) {
+      if (!mbar_wait_warp(&ctl.bar_q, 0, guard, 8)) {
+        ok = false;
+      } else {
+        if (w == 0 || C::Q_TMEM) {
+          const uint8_t* base = (w == 0) ? sDO : sQ;
+          const int ncb = (w == 0) ? DV / 64 : DQK / 64;
+          const uint32_t tdst = tmem + lane_base + ((w == 0) ? C::T_DO : C::T_Q);
+#pragma unroll 1
+          for (int cb = 0; cb < ncb; ++cb) {
+            const uint8_t* row = base + cb * (C::BQ * 128) + r * 128;
+            uint32_t wd[2][16];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) * 16));
+              wd[c / 4][(c % 4) * 4 + 0] = u.x;
+              wd[c / 4][(c % 4) * 4 + 1] = u.y;
+              wd[c / 4][(c % 4) * 4 + 2] = u.z;
+              wd[c / 4][(c % 4) * 4 + 3] = u.w;
+            }
+            tmem_st16(tdst + cb * 32, wd[0]);
+            tmem_st16(tdst + cb * 32 + 16, wd[1]);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive_warp(&ctl.op_tmem);
+      }
+    }
+    for (int it = w; ok && it < NIT; it += 2) {
       const int kt = k0 + it;
       const int j0 = kt * C::BK;
       const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && j0 + C::BK > t * C::BQ + off + p.right) ||

@@ -50,21 +50,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps (issuing nothing)
-// until the phase completes or about `ns` nanoseconds pass. Spinning waiters otherwise take issue
-// slots from the warps sharing their SM sub-partition.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Error word layout (device int): bit 31 set = timeout; low bits = wait site id.
 struct WaitGuard {
   int* err;               // global error word (may be null)
@@ -79,7 +64,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait_sleep(a, parity, 10000u)) return true;  // sleeps at most ~10 us per try
+    // try_wait without a suspend-time hint: measured ~1 % faster on the backward and the forward than
+    // a 10 us hint (the hardware still suspends the thread for a short, system-defined time)
+    if (mbar_try_wait(a, parity)) return true;
     if (*g.abort) return false;
     if (clock64() - t0 > g.limit) {
       *g.abort = 1;
