@@ -189,6 +189,15 @@ def _traffic(kernel_key: str, src_hash: str):
     return None
 
 
+def launches_per_step(p):
+    """Kernels one preprocess / main / postprocess pass launches, by the library's rules: the
+    preprocess, the key-stationary main kernel and either the dQ cast (an fp32 dQ accumulator:
+    Dqk 64 / 128, not deterministic) or the query-stationary dQ pass; with per-head CTAs (group
+    mode b) also the dK and dV casts."""
+    import gqa_flashattention_backward_gb300._native as nat
+    return 3 + (2 if not p.deterministic and p.group_mode == nat.GQA_GROUP_ATOMIC else 0)
+
+
 def run_gpu(args):
     import torch
 
@@ -247,7 +256,7 @@ def run_gpu(args):
         if ev is not None:
             ev[1].record()
         nat.bwd_postprocess(p, o["dq"], o["dk"], o["dv"], c["ws"])
-        n = 3
+        n = launches_per_step(p)
         if c["sink"] is not None:
             nat.dsink(p, c["sink"], c["lse"], o["delta"], o["dsink"])
             n += 1
