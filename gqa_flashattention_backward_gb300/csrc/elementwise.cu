@@ -155,27 +155,29 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
 }
 
 // out row (b, h, s) = dtype(acc row * mul): acc is contiguous fp32 [B, H, S, D], out has the caller's
-// layout; 8 elements (one 16-byte store) per thread-iteration.
-template <typename T>
+// layout; 8 elements (two 16-byte loads, one 16-byte store) per thread-iteration.  Grid y walks the
+// (b, h) pairs and x the S * D / 8 chunks of one pair, so a chunk's row comes from one division by a
+// compile-time constant (64-bit divisions by S and H per chunk kept the kernel instruction-bound).
+template <typename T, int D>
 __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ acc, T* __restrict__ out, int H, int S,
-                                                   int D, Strides st, long long n8, float mul) {
-  const int per_row = D / 8;
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = e / per_row;
-    const int c8 = static_cast<int>(e - row * per_row);
-    const int s = static_cast<int>(row % S);
-    const int h = static_cast<int>((row / S) % H);
-    const int b = static_cast<int>(row / (static_cast<long long>(S) * H));
-    const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * e);
-    const float4 c = __ldg(reinterpret_cast<const float4*>(acc) + 2 * e + 1);
-    uint4 r;
-    constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
-    r.x = pack2<BF>(a.x * mul, a.y * mul);
-    r.y = pack2<BF>(a.z * mul, a.w * mul);
-    r.z = pack2<BF>(c.x * mul, c.y * mul);
-    r.w = pack2<BF>(c.z * mul, c.w * mul);
-    *reinterpret_cast<uint4*>(out + st.row(b, h, s) + 8 * c8) = r;
+                                                   int BH, Strides st, float mul) {
+  constexpr int PER_ROW = D / 8;
+  constexpr bool BF = std::is_same<T, __nv_bfloat16>::value;
+  const int n = S * PER_ROW;  // chunks of one (b, h)
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    const int b = bh / H, h = bh - b * H;
+    const float4* a4 = reinterpret_cast<const float4*>(acc + static_cast<size_t>(bh) * S * D);
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x) {
+      const int si = e / PER_ROW, c8 = e - si * PER_ROW;
+      const float4 a = __ldg(a4 + 2 * static_cast<size_t>(e));
+      const float4 c = __ldg(a4 + 2 * static_cast<size_t>(e) + 1);
+      uint4 r;
+      r.x = pack2<BF>(a.x * mul, a.y * mul);
+      r.y = pack2<BF>(a.z * mul, a.w * mul);
+      r.z = pack2<BF>(c.x * mul, c.y * mul);
+      r.w = pack2<BF>(c.z * mul, c.w * mul);
+      *reinterpret_cast<uint4*>(out + st.row(b, h, si) + 8 * c8) = r;
+    }
   }
 }
 
@@ -260,18 +262,30 @@ cudaError_t launch_preprocess(const Problem& p, int dtype_bf16, const void* o, c
 
 cudaError_t launch_cast(const float* acc, void* out, int B, int H, int S, int D, const Strides& st, float mul,
                         int dtype_bf16, int num_sms, cudaStream_t st_) {
-  const long long n8 = static_cast<long long>(B) * H * S * (D / 8);
-  if (n8 <= 0) return cudaSuccess;
-  long long blocks = (n8 + 255) / 256;
-  const long long cap = static_cast<long long>(num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  if (dtype_bf16)
-    cast_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st_>>>(
-        acc, static_cast<__nv_bfloat16*>(out), H, S, D, st, n8, mul);
-  else
-    cast_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, st_>>>(acc, static_cast<__half*>(out), H, S, D, st,
-                                                                         n8, mul);
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh <= 0 || S <= 0) return cudaSuccess;
+  if (static_cast<long long>(S) * (D / 8) > 0x7fffffffLL || bh > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // about eight 256-thread blocks per SM in all, spread over the (b, h) pairs
+  const long long per_bh = (static_cast<long long>(S) * (D / 8) + 255) / 256;
+  const unsigned gy = static_cast<unsigned>(bh < 65535 ? bh : 65535);
+  long long gx = (static_cast<long long>(num_sms) * 8 + gy - 1) / gy;
+  if (gx > per_bh) gx = per_bh;
+  if (gx < 1) gx = 1;
+  const dim3 grid(static_cast<unsigned>(gx), gy);
+#define GQA_CAST(T, DD)                                                                                 \
+  cast_kernel<T, DD><<<grid, 256, 0, st_>>>(acc, static_cast<T*>(out), H, S, static_cast<int>(bh), st, mul)
+  if (dtype_bf16) {
+    if (D == 64) GQA_CAST(__nv_bfloat16, 64);
+    else if (D == 128) GQA_CAST(__nv_bfloat16, 128);
+    else if (D == 192) GQA_CAST(__nv_bfloat16, 192);
+    else return cudaErrorInvalidValue;
+  } else {
+    if (D == 64) GQA_CAST(__half, 64);
+    else if (D == 128) GQA_CAST(__half, 128);
+    else if (D == 192) GQA_CAST(__half, 192);
+    else return cudaErrorInvalidValue;
+  }
+#undef GQA_CAST
   return cudaGetLastError();
 }
 
