@@ -267,28 +267,39 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < C::BK; c0 += 32) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tS + c0, sv);
-        tmem_ld32(tS + C::BK + c0, dv);
+      const float2 sl22 = make_float2(sl2, sl2), nl2 = make_float2(nlse2, nlse2), nd2 = make_float2(ndlt, ndlt);
+      // dS of the 32 key columns starting at c0 from their S and dP, packed over S's first half: chunk
+      // c0 lands in columns [c0/2, c0/2 + 16), which earlier chunks have already read
+      auto ds_chunk = [&](int c0, const uint32_t (&sv)[32], const uint32_t (&dv)[32]) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float pa = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), sl2, nlse2));
-          float pb = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), sl2, nlse2));
+          // P = exp2(S * scale * log2e - LSE2) and dS = P * (dP - Delta), two columns at a time
+          const float2 x = fma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl22, nl2);
+          float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (need_mask) {
             const int d0 = il + off - j0 - c0;  // diagonal distance to this chunk's first key
-            if (!visible_d(d0 - 2 * e, j0 + c0 + 2 * e < sk.len, p.right, p.window)) pa = 0.f;
-            if (!visible_d(d0 - 2 * e - 1, j0 + c0 + 2 * e + 1 < sk.len, p.right, p.window)) pb = 0.f;
+            if (!visible_d(d0 - 2 * e, j0 + c0 + 2 * e < sk.len, p.right, p.window)) pp.x = 0.f;
+            if (!visible_d(d0 - 2 * e - 1, j0 + c0 + 2 * e + 1 < sk.len, p.right, p.window)) pp.y = 0.f;
           }
-          const float da = pa * (__uint_as_float(dv[2 * e]) + ndlt);
-          const float db = pb * (__uint_as_float(dv[2 * e + 1]) + ndlt);
-          pk[e] = pack2<BF16>(da, db);
+          const float2 d = mul2(pp, add2(make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd2));
+          pk[e] = pack2<BF16>(d.x, d.y);
         }
-        // dS packed over S's first half: chunk c0 lands in columns [c0/2, c0/2 + 16), already read
         tmem_st16(tS + c0 / 2, pk);
-      }
+      };
+      // the two 32-column chunks of the tile: the second one's S and dP load while the first is used
+      static_assert(C::BK == 64, "two 32-column chunks");
+      uint32_t s0[32], d0v[32], s1[32], d1v[32];
+      tmem_ld32_start(tS, s0);
+      tmem_ld32_start(tS + C::BK, d0v);
+      tmem_ld_wait(s0);
+      tmem_ld_wait(d0v);
+      tmem_ld32_start(tS + 32, s1);
+      tmem_ld32_start(tS + C::BK + 32, d1v);
+      ds_chunk(0, s0, d0v);
+      tmem_ld_wait(s1);
+      tmem_ld_wait(d1v);
+      ds_chunk(32, s1, d1v);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(&ctl.sm_done[b]);
