@@ -27,6 +27,9 @@
 // issue #4717 "atomic_add slows down attention backwards due to layout
 // conversions": vectorised atomics against scalar ones).
 //
+// For head dim 64 the stationary K and V tiles are also copied into TMEM and
+// serve as the A operands of S^T and dP^T, and dS^T is packed over dP^T.
+//
 // Warp roles (448 threads): warps 0-3 and 4-7 are two softmax/dS warpgroups
 // (thread r = key row r = TMEM lane r; the first takes query columns [0, BQ/2),
 // the second [BQ/2, BQ)); warps 8-11 dQ drain warpgroup (thread r = query row r);

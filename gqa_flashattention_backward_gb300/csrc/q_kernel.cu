@@ -15,7 +15,9 @@
 // `it` has the TMEM buffer it % 2: while one warpgroup works on its tile the
 // tensor core computes the other's.  Operands live in shared memory in the
 // 128-byte swizzled layout TMA writes; S, dP and dQ accumulate in TMEM; dS is
-// packed to 16 bits over S and feeds the dQ MMA as its A operand.
+// packed to 16 bits over S and feeds the dQ MMA as its A operand.  The
+// stationary dO tile (and Q, where the TMEM columns allow) is copied into TMEM
+// once and is the A operand of dP (and S).
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include <type_traits>
