@@ -110,9 +110,12 @@ __global__ void __launch_bounds__(256) preprocess_kernel(Problem p, const T* __r
         acc = fmaf(x.y, y.y, acc);
       }
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    // the row's eight threads are one aligned group of eight lanes, all active together (a warp's other
+    // rows may have left the loop at the end of the rows): the mask names exactly that group
+    const unsigned grp = 0xFFu << (threadIdx.x & 24);
+    acc += __shfl_xor_sync(grp, acc, 1);
+    acc += __shfl_xor_sync(grp, acc, 2);
+    acc += __shfl_xor_sync(grp, acc, 4);
     int s, il, len;
     if (p.cu_seqlens) {
       s = find_seq(p.cu_seqlens, p.nseqs, i);
