@@ -1,7 +1,8 @@
 """Seeded random configurations: head dims, dtypes, group sizes, masks (causal, sliding window,
 two-sided and right-only local windows, none), sinks, packed batches with empty and one-token
 sequences, keys fewer or more than queries, input scales and every reduction mode, drawn together
-so that combinations no hand-written case names are exercised.  Each is run forward and backward
+so that combinations no hand-written case names are exercised; some draws also take a softmax scale
+other than 1/sqrt(Dqk).  Each is run forward and backward
 through the C ABI and compared element by element with the fp64 oracle on the same rounded
 inputs; rows that see no key (possible when keys are fewer than queries) must have LSE = -inf on
 both sides.  A CPU test checks first that the library's parameter validation accepts every drawn
@@ -69,6 +70,11 @@ def _draw(rng, i):
         if cross:
             kw.update(Sk=rng.randint(1, 450))
     mode = (i // len(MASKS) + i) % len(MODES)
+    # a softmax scale other than 1/sqrt(Dqk) now and then (logits stay well conditioned: their standard
+    # deviation is at most qkv_std^2 * 1.5 = 6)
+    mult = rng.choice([1.0, 1.0, 0.5, 1.5])
+    if mult != 1.0:
+        kw.update(scale=mult * dqk ** -0.5)
     return W.Workload(f"rand{i}", 300 + i, **kw), mode
 
 
@@ -93,6 +99,8 @@ def _id(c):
         parts.append(f"wr{w.window_right}")
     if w.sink:
         parts.append("sink")
+    if w.scale is not None:
+        parts.append(f"x{w.scale * w.Dqk ** 0.5:g}")
     parts.append(f"m{mode}")
     return "-".join(parts)
 
@@ -119,6 +127,7 @@ def test_draws_cover_the_space():
     assert any(not w.causal and not w.window and w.window_right for w in ws)
     assert any(not w.causal and not w.window and not w.window_right for w in ws)
     assert any(w.varlen_lengths and 0 in w.varlen_lengths for w in ws)
+    assert any(w.scale is not None for w in ws)
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=_id)
