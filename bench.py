@@ -627,6 +627,9 @@ PROFILE_WORKLOADS = {
     "varlen": lambda W: W.varlen(),
     "sink_window": lambda W: W.sink_window(),
     "long_context": lambda W: W.long_context(),
+    # the long-context shape at a quarter of its length: a few hundred MB on the device, for captures
+    # that replay a launch many times
+    "long_context_s8192": lambda W: W.shrink(W.long_context(), name="long_context_s8192", S=8192),
 }
 
 
