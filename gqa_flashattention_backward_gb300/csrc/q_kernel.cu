@@ -278,14 +278,17 @@ __global__ void __launch_bounds__(320, 1)
         for (int e = 0; e < 16; ++e) {
           // P = exp2(S * scale * log2e - LSE2) and dS = P * (dP - Delta), two columns at a time
           const float2 x = fma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl22, nl2);
-          float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          if (need_mask) {
-            const int d0 = il + off - j0 - c0;  // diagonal distance to this chunk's first key
-            if (!visible_d(d0 - 2 * e, j0 + c0 + 2 * e < sk.len, p.right, p.window)) pp.x = 0.f;
-            if (!visible_d(d0 - 2 * e - 1, j0 + c0 + 2 * e + 1 < sk.len, p.right, p.window)) pp.y = 0.f;
-          }
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           const float2 d = mul2(pp, add2(make_float2(__uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1])), nd2));
           pk[e] = pack2<BF16>(d.x, d.y);
+        }
+        // masked keys: dS = P * (dP - Delta) is 0 where P is, so their packed halves are cleared (one test
+        // per chunk on the unmasked tiles)
+        if (need_mask) {
+          const int d0 = il + off - j0 - c0;  // diagonal distance to this chunk's first key
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!visible_d(d0 - e, j0 + c0 + e < sk.len, p.right, p.window)) pk[e / 2] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
         }
         tmem_st16(tS + c0 / 2, pk);
       };
