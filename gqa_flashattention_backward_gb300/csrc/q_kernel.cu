@@ -36,10 +36,12 @@ struct QCfg {
   static constexpr int K_BYTES = BK * DQK * 2;
   static constexpr int V_BYTES = BK * DV * 2;
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;  // one K + V stage
+  // the dO tile is read once, by the softmax warps that copy it into TMEM: it is loaded into the last
+  // K/V stage, which takes its first key tile only after that copy (one more stage in flight)
   static constexpr int BUDGET = 220 * 1024;
-  static constexpr int KST_RAW = (BUDGET - Q_BYTES - DO_BYTES) / STAGE_BYTES;
+  static constexpr int KST_RAW = (BUDGET - Q_BYTES) / STAGE_BYTES;
   static constexpr int KST = KST_RAW > 8 ? 8 : KST_RAW;
-  static constexpr int SMEM = 1024 + Q_BYTES + DO_BYTES + KST * STAGE_BYTES;
+  static constexpr int SMEM = 1024 + Q_BYTES + KST * STAGE_BYTES;
   // TMEM: buffer b at b*BUF holds S (BK columns; dS packed over its first half) and dP right after
   // it; the dQ accumulator follows the two buffers
   static constexpr int NBUF = 2;
@@ -55,6 +57,7 @@ struct QCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int THREADS = 320;
   static_assert(KST >= 2, "stages");
+  static_assert(DO_BYTES <= STAGE_BYTES, "the dO tile fits in one K/V stage");
   static_assert(SMEM <= 227 * 1024, "shared memory");
   static_assert(T_DO + DV / 2 <= 512, "tmem");
   static_assert(DQK % 64 == 0, "each warpgroup drains whole 32-column chunks");
@@ -66,7 +69,7 @@ struct QSmemCtl {
   uint64_t s_full[2];   // tensor core -> warpgroup: S and dP of the buffer's tile are in TMEM
   uint64_t sm_done[2];  // warpgroup -> tensor core: dS stored, buffer reusable
   uint64_t acc_done;
-  uint64_t op_tmem;     // softmax warps -> tensor core: dO (and Q) copied into TMEM
+  uint64_t op_tmem;     // softmax warps -> tensor core and producer: dO (and Q) copied into TMEM
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -80,8 +83,8 @@ __global__ void __launch_bounds__(320, 1)
   __shared__ QSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sDO = sQ + C::Q_BYTES;
-  uint8_t* sK0 = sDO + C::DO_BYTES;  // stage st: K at sK0 + st*STAGE_BYTES, V right after K
+  uint8_t* sK0 = sQ + C::Q_BYTES;  // stage st: K at sK0 + st*STAGE_BYTES, V right after K
+  uint8_t* sDO = sK0 + (C::KST - 1) * C::STAGE_BYTES;  // until it is in TMEM
 
   const int h = blockIdx.x;
   const int s = blockIdx.z;
@@ -140,6 +143,8 @@ __global__ void __launch_bounds__(320, 1)
       for (int it = 0; it < NIT; ++it) {
         const int st = it % C::KST;
         if (it >= C::KST && !mbar_wait(&ctl.kv_empty[st], ((it / C::KST) - 1) & 1, guard, 1)) break;
+        // the last stage holds dO until the softmax warps have copied it into TMEM
+        if (it == C::KST - 1 && !mbar_wait(&ctl.op_tmem, 0, guard, 10)) break;
         uint8_t* sK = sK0 + st * C::STAGE_BYTES;
         uint8_t* sV = sK + C::K_BYTES;
         mbar_expect_tx(&ctl.kv_full[st], C::K_BYTES + C::V_BYTES);
