@@ -460,23 +460,39 @@ __global__ void __launch_bounds__(448, 1)
           tmem_ld_half<C::BQ>(tmem + lane_base + C::T_DQ, v);
           tc_fence_before();
           mbar_arrive_warp(&ctl.dq_empty);
-          if (r == 0 && nbulk > 0) bulk_wait_read0();  // the previous tile's reduce has read the staging
-          named_bar_sync(1, 128);
-#pragma unroll
-          for (int i = 0; i < C::BQ; ++i) tst[i * DQK + r] = __uint_as_float(v[i]);
           const int row0 = t * C::BQ;
           const int nvalid = sq.len - row0 < C::BQ ? sq.len - row0 : C::BQ;
           float* gdst = p.dq_acc + ((static_cast<size_t>(sq.b) * p.Hq + h) * p.S + sq.start + row0) * DQK;
-          if (dq_mode == kDqBulk || dq_mode == kDqStore) {  // kDqStore: the same copy, stored
-            fence_async_smem();
-            named_bar_sync(1, 128);
-            if (r == 0) {  // the tile's rows are contiguous in the accumulator: one bulk reduce
-              if (dq_mode == kDqStore) bulk_store_f32(gdst, tst, static_cast<uint32_t>(nvalid) * DQK * 4);
-              else bulk_reduce_add_f32(gdst, tst, static_cast<uint32_t>(nvalid) * DQK * 4);
-              bulk_commit();
+          if (dq_mode == kDqBulk || dq_mode == kDqStore) {  // kDqStore: the same copies, stored
+            // two halves of BQ/2 query rows, each staged in its own half of the buffer and reduced by its
+            // own bulk operation: a half is written while the other half's previous reduce still reads
+            // shared memory, instead of every tile waiting for the whole previous reduce
+            constexpr int HQ = C::BQ / 2;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float* hst = tst + hh * HQ * DQK;
+              // one bulk group per half (empty when the half has no valid row): the group two back read
+              // this half of the buffer
+              if (r == 0 && nbulk >= 2) bulk_wait_read1();
+              named_bar_sync(1, 128);
+#pragma unroll
+              for (int i = 0; i < HQ; ++i) hst[i * DQK + r] = __uint_as_float(v[hh * HQ + i]);
+              fence_async_smem();
+              named_bar_sync(1, 128);
+              const int nv = nvalid - hh * HQ < 0 ? 0 : (nvalid - hh * HQ > HQ ? HQ : nvalid - hh * HQ);
+              if (r == 0) {  // the half's rows are contiguous in the accumulator
+                if (nv > 0) {
+                  if (dq_mode == kDqStore) bulk_store_f32(gdst + hh * HQ * DQK, hst, static_cast<uint32_t>(nv) * DQK * 4);
+                  else bulk_reduce_add_f32(gdst + hh * HQ * DQK, hst, static_cast<uint32_t>(nv) * DQK * 4);
+                }
+                bulk_commit();
+              }
+              ++nbulk;
             }
-            ++nbulk;
           } else {
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int i = 0; i < C::BQ; ++i) tst[i * DQK + r] = __uint_as_float(v[i]);
             named_bar_sync(1, 128);
             const float4* s4 = reinterpret_cast<const float4*>(tst);
             for (int idx = r; idx < nvalid * (DQK / 4); idx += 128) {
