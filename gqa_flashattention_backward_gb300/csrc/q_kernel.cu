@@ -174,11 +174,14 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = mbar_wait_warp(&ctl.bar_q, 0, guard, 2);
       if (ok && NIT > 0) ok = mbar_wait_warp(&ctl.op_tmem, 0, guard, 9);
       // S and dP of tile `it` into buffer it % 2, once the tile two earlier has left it
-      auto issue_s = [&](int it) -> bool {
+      // `waited`: the caller has already waited for the K/V tile and for the buffer's previous tile
+      auto issue_s = [&](int it, bool waited) -> bool {
         const int st = it % C::KST, b = it % C::NBUF;
-        if (!mbar_wait_warp(&ctl.kv_full[st], (it / C::KST) & 1, guard, 3)) return false;
-        if (it >= C::NBUF && !mbar_wait_warp(&ctl.sm_done[b], ((it - C::NBUF) / C::NBUF) & 1, guard, 4))
-          return false;
+        if (!waited) {
+          if (!mbar_wait_warp(&ctl.kv_full[st], (it / C::KST) & 1, guard, 3)) return false;
+          if (it >= C::NBUF && !mbar_wait_warp(&ctl.sm_done[b], ((it - C::NBUF) / C::NBUF) & 1, guard, 4))
+            return false;
+        }
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * C::STAGE_BYTES);
         const uint64_t dK = sdesc_sw128(aK, 16, 1024);
@@ -210,12 +213,20 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit(&ctl.kv_empty[st]);
         return true;
       };
-      for (int it = 0; ok && it < C::NBUF && it < NIT; ++it) ok = issue_s(it);
+      for (int it = 0; ok && it < C::NBUF && it < NIT; ++it) ok = issue_s(it, false);
       // in the order the warpgroups release the buffers: tile it's accumulation, then the
-      // tile that takes its buffer next
+      // tile that takes its buffer next (the accumulation's wait for tile it is also the wait for the
+      // buffer).  With a deep K/V ring the next tile's K/V wait comes first, while the softmax still
+      // works on tile it; with a shallow one that load may still be in flight, and the accumulation
+      // goes first.
+      constexpr bool EARLY_KV = C::KST >= 6;
       for (int it = 0; ok && it < NIT; ++it) {
+        const int nx = it + C::NBUF;
+        const bool more = nx < NIT;
+        if (EARLY_KV && more && !mbar_wait_warp(&ctl.kv_full[nx % C::KST], (nx / C::KST) & 1, guard, 3)) break;
         if (!issue_acc(it)) break;
-        if (it + C::NBUF < NIT && !issue_s(it + C::NBUF)) break;
+        if (!EARLY_KV && more && !mbar_wait_warp(&ctl.kv_full[nx % C::KST], (nx / C::KST) & 1, guard, 3)) break;
+        if (more && !issue_s(nx, true)) break;
       }
       umma_commit(&ctl.acc_done);
     }
