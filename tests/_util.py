@@ -66,3 +66,17 @@ def oracle_full(w, inputs):
     g = orc.backward(pb, f64(q), f64(k), f64(v), o, lse, f64(do), sink64)
     g["o"], g["lse"] = o, lse
     return g
+
+
+
+def oracle_backward_on_stored(w, inputs, ref):
+    """The oracle backward on the O the GPU backward reads: the oracle's O rounded to the input dtype
+    (and its LSE).  Delta is defined on O as stored (tilelang-ascend PR #1638 "Add GQA Sink Backward
+    BHSD", 4->2 commit: Phase0(Delta) = sum(O*dO)); with few keys per row, or many rows in dsink, the
+    rounding of O alone moves dQ, dK and dsink past 2e-2 max|ref| in bf16, so a backward check that
+    should see only the kernels' own arithmetic gives both sides the same stored O."""
+    q, k, v, do, sink = inputs
+    o_st = f64(torch.as_tensor(ref["o"]).to(w.dtype))
+    sink64 = f64(sink) if sink is not None else None
+    g = orc.backward(problem_of(w), f64(q), f64(k), f64(v), o_st, ref["lse"], f64(do), sink64)
+    return g

@@ -1,7 +1,8 @@
 """Packed batches with many sequences: up to 256 sequences the main kernel runs them longest first,
 through an order the preprocess writes into the workspace; above that it takes them in packing
 order.  Both sides of that boundary, and a batch of 600 short sequences (empty and one-token ones
-among them), in several accumulation modes, against the fp64 oracle."""
+among them), in several accumulation modes, against the fp64 oracle: the forward's O and LSE, and the
+backward on the same stored O and LSE on both sides."""
 import random
 
 import pytest
@@ -9,7 +10,7 @@ import torch
 
 from gqa_flashattention_backward_gb300 import _native as nat
 from gqa_flashattention_backward_gb300 import workloads as W
-from tests._util import assert_close, f64, gpu_run, oracle_full
+from tests._util import assert_close, f64, gpu_run, oracle_backward_on_stored, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +49,10 @@ def test_many_sequences(case):
     res = gpu_run(w, inputs, **mode)
     assert_close(f"{case}:o", f64(res["o"]), ref["o"])
     assert_close(f"{case}:lse", f64(res["lse"]), ref["lse"], rtol=1e-3, atol=1e-3)
+    # the backward on the same stored O and LSE on both sides
+    ref_b = oracle_backward_on_stored(w, inputs, ref)
+    res_b = gpu_run(w, inputs, o_lse=(ref["o"], ref["lse"]), **mode)
     for n in ("dq", "dk", "dv"):
-        assert_close(f"{case}:{n}", f64(res[n]), ref[n])
+        assert_close(f"{case}:{n}", f64(res_b[n]), ref_b[n])
     if w.sink:
-        assert_close(f"{case}:dsink", f64(res["dsink"]), ref["dsink"])
+        assert_close(f"{case}:dsink", f64(res_b["dsink"]), ref_b["dsink"])

@@ -4,8 +4,9 @@ sequences, keys fewer or more than queries, input scales and every reduction mod
 so that combinations no hand-written case names are exercised; some draws also take a softmax scale
 other than 1/sqrt(Dqk).  Each is run forward and backward
 through the C ABI and compared element by element with the fp64 oracle on the same rounded
-inputs; rows that see no key (possible when keys are fewer than queries) must have LSE = -inf on
-both sides.  A CPU test checks first that the library's parameter validation accepts every drawn
+inputs: O and LSE from the GPU forward against the oracle's (rows that see no key, possible when keys
+are fewer than queries, must have LSE = -inf on both sides), and the backward against the oracle
+backward on the same stored O and LSE.  A CPU test checks first that the library's parameter validation accepts every drawn
 configuration, so that a GPU failure is a numerical one."""
 import random
 
@@ -15,7 +16,7 @@ import torch
 
 from gqa_flashattention_backward_gb300 import _native as nat
 from gqa_flashattention_backward_gb300 import workloads as W
-from tests._util import assert_close, f64, gpu_run, oracle_full
+from tests._util import assert_close, f64, gpu_run, oracle_backward_on_stored, oracle_full
 
 SEED = 5281
 COUNT = 24
@@ -145,12 +146,17 @@ def test_random_config(cfg):
     w, mode = cfg
     inputs = W.make_inputs(w)
     ref = oracle_full(w, inputs)
+    # forward: O and LSE against the oracle's
     res = gpu_run(w, inputs, **MODES[mode])
     lse, rlse = f64(res["lse"]), ref["lse"]
     empty = np.isneginf(rlse)
     assert np.array_equal(np.isneginf(lse), empty), f"{w.name}: rows without keys differ"
     assert_close(f"{w.name}:lse", lse[~empty], rlse[~empty], rtol=1e-3, atol=1e-3)
-    for n in ("o", "dq", "dk", "dv"):
-        assert_close(f"{w.name}:{n}", f64(res[n]), ref[n])
+    assert_close(f"{w.name}:o", f64(res["o"]), ref["o"])
+    # backward: both sides on the same stored O and LSE
+    ref_b = oracle_backward_on_stored(w, inputs, ref)
+    res_b = gpu_run(w, inputs, o_lse=(ref["o"], ref["lse"]), **MODES[mode])
+    for n in ("dq", "dk", "dv"):
+        assert_close(f"{w.name}:{n}", f64(res_b[n]), ref_b[n])
     if w.sink:
-        assert_close(f"{w.name}:dsink", f64(res["dsink"]), ref["dsink"])
+        assert_close(f"{w.name}:dsink", f64(res_b["dsink"]), ref_b["dsink"])
