@@ -5,7 +5,10 @@
 // One CTA owns two 128-row query tiles of one query head; softmax warpgroup w
 // (warps 4w..4w+3, thread r = query row r of tile w = TMEM lane r) keeps its own
 // running row maximum, row sum and O accumulator, so the two tiles need no
-// exchange and take turns on the tensor core.  Per key tile of BK keys:
+// exchange and take turns on the tensor core.  The CTA loads every key tile
+// either query tile can see; with 128-key tiles each warpgroup (and the MMA
+// warp on its behalf) skips the tiles that its own rows cannot see (a sliding
+// window's far edge, the other tile's causal diagonal).  Per key tile of BK keys:
 //
 //   S_w  = Q_w . K^T                     (tcgen05, fp32 in TMEM)
 //   m_ref = reference maximum of S_w * scale * log2(e) (below)
@@ -60,6 +63,10 @@ struct FwdCfg {
   // 192: its 64-key S tiles are short, and the tensor core rather than the softmax sets the pace).
   static constexpr uint32_t WG_COLS = BK + DV;
   static constexpr bool SEP_P = DQK == 64;
+  // each warpgroup on its own key tiles only (128-key tiles).  With 64-key tiles (head dim 192) the MMA
+  // warp issues an S MMA every ~32 cycles and sets the pace, and the per-tile range tests cost more
+  // than the two masked tiles per pair they save: both warpgroups then run the union
+  static constexpr bool OWN_RANGES = BK == 128;
   static constexpr uint32_t P_COL = 2 * WG_COLS;  // SEP_P: P of warpgroup w at P_COL + w * BK / 2
   static constexpr uint32_t TMEM_COLS = 512;
   // P <= 2^TAU: m_ref moves only when a tile's row sum of P exceeds P_MAX = 2^TAU.  fp16 exponentiates
@@ -118,16 +125,28 @@ __global__ void __launch_bounds__(384, 1)
   const int npair = (sq.len + 2 * C::BQ - 1) / (2 * C::BQ);
   const int tp = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tile pairs first
   if (tp >= npair) return;
-  // key tiles either query tile of the pair can see (a tile only one of them sees is masked for the other)
-  int k0, k1, ka, kb;
-  kv_tiles_for_q_tile(2 * tp, sq.len, sk.len, C::BK, p.right, p.window, &k0, &k1);
-  kv_tiles_for_q_tile(2 * tp + 1, sq.len, sk.len, C::BK, p.right, p.window, &ka, &kb);
-  if (2 * tp + 1 < (sq.len + C::BQ - 1) / C::BQ) {
-    if (ka < k0) k0 = ka;
-    if (kb > k1) k1 = kb;
+  // each query tile's own key tiles [lo_w, hi_w) (none for a tile past the sequence's end); the CTA loads
+  // their union [k0, k1), and warpgroup w works (and the MMA warp issues for it) only on its own tiles,
+  // local indices jlo_w <= j < jhi_w of the union
+  int lo[2], hi[2];
+  kv_tiles_for_q_tile(2 * tp, sq.len, sk.len, C::BK, p.right, p.window, &lo[0], &hi[0]);
+  lo[1] = hi[1] = 0;
+  if (2 * tp + 1 < (sq.len + C::BQ - 1) / C::BQ)
+    kv_tiles_for_q_tile(2 * tp + 1, sq.len, sk.len, C::BK, p.right, p.window, &lo[1], &hi[1]);
+  int k0 = 0, k1 = 0;
+  bool any = false;
+  for (int w = 0; w < 2; ++w) {
+    if (hi[w] <= lo[w]) continue;
+    k0 = any && k0 < lo[w] ? k0 : lo[w];
+    k1 = any && k1 > hi[w] ? k1 : hi[w];
+    any = true;
   }
-  if (k1 < k0) k1 = k0;
   const int n = k1 - k0;
+  // (scalars, so that no runtime index puts them in local memory)
+  const int jlo0 = C::OWN_RANGES && hi[0] > lo[0] ? lo[0] - k0 : 0;
+  const int jhi0 = !C::OWN_RANGES ? n : hi[0] > lo[0] ? hi[0] - k0 : 0;
+  const int jlo1 = C::OWN_RANGES && hi[1] > lo[1] ? lo[1] - k0 : 0;
+  const int jhi1 = !C::OWN_RANGES ? n : hi[1] > lo[1] ? hi[1] - k0 : 0;
   const int g = h / p.G;
   const int zq = sq.b * p.Hq + h;
 
@@ -221,7 +240,15 @@ __global__ void __launch_bounds__(384, 1)
                   idS, kk > 0);
         umma_commit(&ctl.s_full[w]);
       };
-      // O_w += P_w . V of key tile j (A = P_w in TMEM, B = V read MN-major)
+      // the two ranges packed as 16-bit halves (n <= 65535 key tiles), for the MMA warp's 24 registers
+      const uint32_t r0 = static_cast<uint32_t>(jlo0) | (static_cast<uint32_t>(jhi0) << 16);
+      const uint32_t r1 = static_cast<uint32_t>(jlo1) | (static_cast<uint32_t>(jhi1) << 16);
+      // O_w += P_w . V of key tile j (A = P_w in TMEM, B = V read MN-major); the warpgroup's first tile
+      // overwrites O
+      auto first = [&](int w) -> int {
+        if constexpr (C::OWN_RANGES) return static_cast<int>((w ? r1 : r0) & 0xffffu);
+        else return 0;
+      };
       auto issue_pv = [&](int w, int j) {
         const int vs = j % C::VST;
         const uint64_t dVmn = sdesc_sw128(smem_u32(sV0 + vs * C::V_BYTES), C::BK * 128, 1024);
@@ -229,17 +256,32 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tP = C::SEP_P ? tmem + C::P_COL + w * (C::BK / 2) : tmem + w * C::WG_COLS;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)
-          umma_ts(tO, tP + kk * 8, desc_advance(dVmn, kk * 2048), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tO, tP + kk * 8, desc_advance(dVmn, kk * 2048), idPV, (j > first(w) || kk > 0) ? 1u : 0u);
       };
+      auto mine = [&](int w, int j) -> bool {
+        if constexpr (C::OWN_RANGES) {
+          const uint32_t r = w ? r1 : r0;
+          return j >= static_cast<int>(r & 0xffffu) && j < static_cast<int>(r >> 16);
+        } else {
+          return true;
+        }
+      };
+      auto phase = [&](int w, int j) -> uint32_t { return static_cast<uint32_t>(j - first(w)) & 1u; };
       if (ok && n > 0) {
         ok = mbar_wait_warp(&ctl.k_full[0], 0, guard, 3);
         if (ok) {
           tc_fence_after();
-          issue_s(0, 0);
-          issue_s(1, 0);
+          if constexpr (C::OWN_RANGES) {
+            for (int w = 0; w < 2; ++w)
+              if (mine(w, 0)) issue_s(w, 0);
+          } else {
+            issue_s(0, 0);
+            issue_s(1, 0);
+          }
           umma_commit(&ctl.k_empty[0]);
         }
       }
+      // every barrier of warpgroup w completes one phase per tile of its own: phase(w, j)
       if constexpr (C::SEP_P) {
         // per key tile j, in the order the two warpgroups (half a tile apart) get there: S_0 of j + 1
         // once warpgroup 0 has read S_0 of j; P_1 . V of j - 1; S_1 of j + 1; P_0 . V of j
@@ -249,8 +291,11 @@ __global__ void __launch_bounds__(384, 1)
           if (next) {
             if (!mbar_wait_warp(&ctl.k_full[kn], ((j + 1) / C::KST) & 1, guard, 3)) { ok = false; break; }
             for (int w = 0; w < 2; ++w) {
-              if (!mbar_wait_warp(&ctl.s_free[w], j & 1, guard, 9)) { ok = false; break; }
-              tc_fence_after();
+              if (!mine(w, j + 1)) continue;
+              if (mine(w, j)) {  // S_w of tile j read before the next S_w overwrites it
+                if (!mbar_wait_warp(&ctl.s_free[w], phase(w, j), guard, 9)) { ok = false; break; }
+                tc_fence_after();
+              }
               issue_s(w, j + 1);
             }
             if (!ok) break;
@@ -258,7 +303,8 @@ __global__ void __launch_bounds__(384, 1)
           }
           if (!mbar_wait_warp(&ctl.v_full[j % C::VST], (j / C::VST) & 1, guard, 8)) { ok = false; break; }
           for (int w = 0; w < 2; ++w) {
-            if (!mbar_wait_warp(&ctl.p_full[w], j & 1, guard, 5)) { ok = false; break; }
+            if (!mine(w, j)) continue;
+            if (!mbar_wait_warp(&ctl.p_full[w], phase(w, j), guard, 5)) { ok = false; break; }
             tc_fence_after();
             issue_pv(w, j);
             umma_commit(&ctl.pv_done[w]);
@@ -266,7 +312,8 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           umma_commit(&ctl.v_empty[j % C::VST]);
         }
-      } else {
+      } else if constexpr (!C::OWN_RANGES) {
+        // both warpgroups on every key tile of the union
         for (int j = 0; ok && j < n; ++j) {
           const bool next = j + 1 < n;
           const int kn = (j + 1) % C::KST;
@@ -292,6 +339,38 @@ __global__ void __launch_bounds__(384, 1)
           umma_commit(&ctl.v_empty[j % C::VST]);
           if (next) umma_commit(&ctl.k_empty[kn]);
         }
+      } else {
+        for (int j = 0; ok && j < n; ++j) {
+          const bool next = j + 1 < n;
+          const int kn = (j + 1) % C::KST;
+          if (!mbar_wait_warp(&ctl.v_full[j % C::VST], (j / C::VST) & 1, guard, 8)) break;
+          bool k_ready = false;
+          for (int w = 0; w < 2; ++w) {
+            // P_w of tile j in TMEM over S_w: its P.V, then S_w of the next tile over the same columns
+            // (tcgen05.mma runs in issue order, so P.V has read P before S overwrites it)
+            if (mine(w, j)) {
+              if (!mbar_wait_warp(&ctl.p_full[w], phase(w, j), guard, 5)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_pv(w, j);
+            }
+            if (next && mine(w, j + 1)) {
+              if (!k_ready && !mbar_wait_warp(&ctl.k_full[kn], ((j + 1) / C::KST) & 1, guard, 3)) {
+                ok = false;
+                break;
+              }
+              k_ready = true;
+              issue_s(w, j + 1);
+            }
+          }
+          if (!ok) break;
+          // a K stage no warpgroup reads has landed all the same before it is handed back
+          if (next && !k_ready && !mbar_wait_warp(&ctl.k_full[kn], ((j + 1) / C::KST) & 1, guard, 3)) break;
+          umma_commit(&ctl.v_empty[j % C::VST]);
+          if (next) umma_commit(&ctl.k_empty[kn]);
+        }
       }
       umma_commit(&ctl.acc_done);
     }
@@ -312,14 +391,16 @@ __global__ void __launch_bounds__(384, 1)
     float mref = sink2;
     float l = sink ? 1.f : 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int j0 = (k0 + j) * C::BK;
+    // this warpgroup's own key tiles: nw of them from key tile kw (local index jl)
+    const int kw = k0 + (w ? jlo1 : jlo0), nw = w ? jhi1 - jlo1 : jhi0 - jlo0;
+    for (int jl = 0; jl < nw; ++jl) {
+      const int j0 = (kw + jl) * C::BK;
       const int i0 = (2 * tp + w) * C::BQ;
       // some key of the tile past the sequence's end, right of the first row's reach or left of the last
-      // row's window (this covers tiles that only the other query tile of the pair sees)
+      // row's window
       const bool need_mask = (j0 + C::BK > sk.len) || (p.right > 0 && j0 + C::BK > i0 + off + p.right) ||
                              (p.window > 0 && i0 + C::BQ - 1 + off - j0 >= p.window);
-      if (!mbar_wait_warp(&ctl.s_full[w], j & 1, guard, 6)) {
+      if (!mbar_wait_warp(&ctl.s_full[w], jl & 1, guard, 6)) {
         ok = false;
         break;
       }
@@ -428,8 +509,8 @@ __global__ void __launch_bounds__(384, 1)
         };
         float t = pass((mref == -INFINITY) ? 0.f : mref);
         // separate P: P . V of the previous tile has finished reading P and adding into O
-        if (C::SEP_P && j > 0) {
-          if (!mbar_wait_warp(&ctl.pv_done[w], (j - 1) & 1, guard, 10)) return false;
+        if (C::SEP_P && jl > 0) {
+          if (!mbar_wait_warp(&ctl.pv_done[w], (jl - 1) & 1, guard, 10)) return false;
           tc_fence_after();
         }
         // every P of the tile is at most its row sum: a sum within 2^TAU keeps P <= 2^TAU.  Above it (or
@@ -441,7 +522,7 @@ __global__ void __launch_bounds__(384, 1)
           const float mnew = fmaxf(mref, tile_max());
           const float f = (mref == -INFINITY) ? 0.f : ex2_approx(mref - mnew);  // nothing accumulated yet: 0
           l *= f;
-          if (j > 0) {
+          if (jl > 0) {
 #pragma unroll 1
             for (int c0 = 0; c0 < DV; c0 += 16) {
               uint32_t o[16];
@@ -476,7 +557,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll 1
       for (int c0 = 0; c0 < DV; c0 += 32) {
         uint32_t v[32];
-        if (n > 0) tmem_ld32(tO + c0, v);  // all lanes: .sync.aligned
+        if (nw > 0) tmem_ld32(tO + c0, v);  // all lanes: .sync.aligned
         else
           for (int e = 0; e < 32; ++e) v[e] = 0u;
         if (valid) {

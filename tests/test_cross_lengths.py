@@ -41,6 +41,11 @@ CASES = {
                                      dtype=torch.bfloat16, qkv_std=0.5),
     "decode64": lambda: W.Workload("x_decode64", 46, B=2, Hq=8, Hkv=2, S=1, Sk=300, Dqk=64, Dv=64,
                                    dtype=torch.float16),
+    # the forward's first pair of 128-row query tiles: the first tile sees no key, the second some
+    "morequeries128": lambda: W.Workload("x_moreq128", 47, B=1, Hq=4, Hkv=2, S=300, Sk=130, Dqk=128, Dv=128,
+                                         dtype=torch.bfloat16),
+    "morequeries192_sink": lambda: W.Workload("x_moreq192s", 48, B=1, Hq=4, Hkv=1, S=300, Sk=100, Dqk=192,
+                                              Dv=128, dtype=torch.bfloat16, sink=True, qkv_std=0.5),
 }
 
 
