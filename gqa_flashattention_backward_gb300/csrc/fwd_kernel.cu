@@ -125,28 +125,16 @@ __global__ void __launch_bounds__(384, 1)
   const int npair = (sq.len + 2 * C::BQ - 1) / (2 * C::BQ);
   const int tp = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tile pairs first
   if (tp >= npair) return;
-  // each query tile's own key tiles [lo_w, hi_w) (none for a tile past the sequence's end); the CTA loads
-  // their union [k0, k1), and warpgroup w works (and the MMA warp issues for it) only on its own tiles,
-  // local indices jlo_w <= j < jhi_w of the union
-  int lo[2], hi[2];
-  kv_tiles_for_q_tile(2 * tp, sq.len, sk.len, C::BK, p.right, p.window, &lo[0], &hi[0]);
-  lo[1] = hi[1] = 0;
-  if (2 * tp + 1 < (sq.len + C::BQ - 1) / C::BQ)
-    kv_tiles_for_q_tile(2 * tp + 1, sq.len, sk.len, C::BK, p.right, p.window, &lo[1], &hi[1]);
-  int k0 = 0, k1 = 0;
-  bool any = false;
-  for (int w = 0; w < 2; ++w) {
-    if (hi[w] <= lo[w]) continue;
-    k0 = any && k0 < lo[w] ? k0 : lo[w];
-    k1 = any && k1 > hi[w] ? k1 : hi[w];
-    any = true;
+  // the union [k0, k0 + n) of the two query tiles' key tiles, which the CTA loads; with OWN_RANGES
+  // warpgroup w works (and the MMA warp issues for it) only on its own tiles, local indices
+  // jlo_w <= j < jhi_w of the union, otherwise both on all n (scalars, so that no runtime index puts
+  // them in local memory)
+  int k0, n, jlo0, jhi0, jlo1, jhi1;
+  fwd_pair_tiles(tp, sq.len, sk.len, C::BK, p.right, p.window, &k0, &n, &jlo0, &jhi0, &jlo1, &jhi1);
+  if constexpr (!C::OWN_RANGES) {
+    jlo0 = jlo1 = 0;
+    jhi0 = jhi1 = n;
   }
-  const int n = k1 - k0;
-  // (scalars, so that no runtime index puts them in local memory)
-  const int jlo0 = C::OWN_RANGES && hi[0] > lo[0] ? lo[0] - k0 : 0;
-  const int jhi0 = !C::OWN_RANGES ? n : hi[0] > lo[0] ? hi[0] - k0 : 0;
-  const int jlo1 = C::OWN_RANGES && hi[1] > lo[1] ? lo[1] - k0 : 0;
-  const int jhi1 = !C::OWN_RANGES ? n : hi[1] > lo[1] ? hi[1] - k0 : 0;
   const int g = h / p.G;
   const int zq = sq.b * p.Hq + h;
 

@@ -1,5 +1,5 @@
-"""The tile ranges the kernels loop over (q_tiles_for_kv_tile, kv_tiles_for_q_tile in the CUDA
-path's common.cuh), compiled for the host and checked against brute-force visibility: every tile
+"""The tile ranges the kernels loop over (q_tiles_for_kv_tile, kv_tiles_for_q_tile and the forward's
+fwd_pair_tiles in the CUDA path's common.cuh), compiled for the host and checked against brute-force visibility: every tile
 holding a visible (query, key) pair lies in the range (a miss would silently drop gradient terms),
 and the range is exactly the span of those tiles (no work on tiles that see nothing).  Covers
 causal / non-causal, left and right windows, more or fewer keys than queries (bottom-right
@@ -76,3 +76,37 @@ def test_tile_ranges_exact(ranges_bin):
             assert (a, b) == (int(hit.min()), int(hit.max()) + 1), case
         else:
             assert a == b, case  # nothing visible: an empty range
+
+
+def test_forward_pair_tiles(ranges_bin):
+    """The forward's CTA takes a pair of 128-row query tiles: it loads the union of their key tiles,
+    and each query tile's warpgroup works on its own part only.  Each own part must be exactly the
+    span of key tiles holding a key visible to that query tile's rows (empty if none, or if the
+    sequence has no second tile), and the union exactly the span of the two parts."""
+    lines, meta = [], []
+    for lq, lk, right, window in _cases(500, 11):
+        for bk in (64, 128):
+            for tp in range((lq + 255) // 256):
+                lines.append(f"f {tp} {lq} {lk} {bk} {right} {window}")
+                meta.append((tp, lq, lk, bk, right, window))
+    res = subprocess.run([ranges_bin], input="\n".join(lines) + "\n", capture_output=True, text=True, check=True)
+    got = [tuple(map(int, ln.split())) for ln in res.stdout.strip().split("\n")]
+    assert len(got) == len(meta)
+    masks = {}
+    for (tp, lq, lk, bk, right, window), (k0, n, jlo0, jhi0, jlo1, jhi1) in zip(meta, got):
+        m = masks.setdefault((lq, lk, right, window), visible(lq, lk, right, window))
+        case = (tp, lq, lk, bk, right, window, (k0, n, jlo0, jhi0, jlo1, jhi1))
+        spans = []
+        for w, (jlo, jhi) in enumerate(((jlo0, jhi0), (jlo1, jhi1))):
+            qt = 2 * tp + w
+            hit = np.nonzero(m[qt * 128:(qt + 1) * 128, :].any(axis=0))[0] // bk if qt * 128 < lq else np.array([])
+            assert 0 <= jlo <= jhi <= n, case
+            if hit.size:
+                assert (k0 + jlo, k0 + jhi) == (int(hit.min()), int(hit.max()) + 1), case
+                spans.append((k0 + jlo, k0 + jhi))
+            else:
+                assert (jlo, jhi) == (0, 0), case
+        if spans:
+            assert (k0, k0 + n) == (min(a for a, _ in spans), max(b for _, b in spans)), case
+        else:
+            assert n == 0, case
