@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <type_traits>
 #include "common.cuh"
+#include "fwd_tiles.cuh"
 #include "umma.cuh"
 #include "launch.h"
 

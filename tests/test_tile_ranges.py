@@ -1,5 +1,5 @@
 """The tile ranges the kernels loop over (q_tiles_for_kv_tile, kv_tiles_for_q_tile and the forward's
-fwd_pair_tiles in the CUDA path's common.cuh), compiled for the host and checked against brute-force visibility: every tile
+fwd_pair_tiles in the CUDA path's common.cuh and fwd_tiles.cuh), compiled for the host and checked against brute-force visibility: every tile
 holding a visible (query, key) pair lies in the range (a miss would silently drop gradient terms),
 and the range is exactly the span of those tiles (no work on tiles that see nothing).  Covers
 causal / non-causal, left and right windows, more or fewer keys than queries (bottom-right

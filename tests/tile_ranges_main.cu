@@ -1,4 +1,4 @@
-// Host driver for the tile-range bookkeeping of the CUDA path (common.cuh): reads lines
+// Host driver for the tile-range bookkeeping of the CUDA path (common.cuh, fwd_tiles.cuh): reads lines
 // "kind tile len_q len_k rows right window" from stdin and prints the range "first end" that
 //   kind q: q_tiles_for_kv_tile -- query tiles of `rows` rows that may see the 128-key tile `tile`
 //   kind k: kv_tiles_for_q_tile -- key tiles of `rows` keys that the 128-row query tile `tile` may see
@@ -7,6 +7,7 @@
 // The kernels visit only these tiles, so a range that misses a visible tile drops gradient terms.
 #include <cstdio>
 #include "common.cuh"
+#include "fwd_tiles.cuh"
 
 int main() {
   char kind;
