@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(384, 1)
                   idS, kk > 0);
         umma_commit(&ctl.s_full[w]);
       };
-      // the two ranges packed as 16-bit halves (n <= 65535 key tiles), for the MMA warp's 24 registers
+      // the two ranges packed as 16-bit halves, for the MMA warp's 24 registers (n <= 65535 128-key tiles:
+      // the parameter check rejects longer sequences)
       const uint32_t r0 = static_cast<uint32_t>(jlo0) | (static_cast<uint32_t>(jhi0) << 16);
       const uint32_t r1 = static_cast<uint32_t>(jlo1) | (static_cast<uint32_t>(jhi1) << 16);
       // O_w += P_w . V of key tile j (A = P_w in TMEM, B = V read MN-major); the warpgroup's first tile
