@@ -42,6 +42,44 @@ def preferred_red_mode(Dqk: int) -> int:
     return GQA_RED_BULK
 
 
+def _validate(q, k, v, **named):
+    """What the C ABI cannot see through its raw pointers: every tensor's dtype, shape and device.
+    `named`: any of o, do, dq, dk, dv (q's dtype), lse, delta (fp32 [B, Hq, S], contiguous), sink,
+    dsink (fp32 [Hq], contiguous), cu_seqlens, cu_seqlens_k (int32, 1-D, contiguous); None is skipped.
+    Raises ValueError naming the first tensor that does not fit."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, S, D]")
+    B, Hq, S, Dqk = q.shape
+    Hkv, Sk, Dv = k.shape[1], k.shape[2], v.shape[3]
+    if k.shape[0] != B or k.shape[3] != Dqk or tuple(v.shape[:3]) != (B, Hkv, Sk):
+        raise ValueError(f"k {tuple(k.shape)} and v {tuple(v.shape)} do not match q {tuple(q.shape)}: "
+                         "expected k [B, Hkv, Sk, Dqk] and v [B, Hkv, Sk, Dv]")
+    f32 = torch.float32
+    want = dict(o=((B, Hq, S, Dv), q.dtype, False), do=((B, Hq, S, Dv), q.dtype, False),
+                dq=((B, Hq, S, Dqk), q.dtype, False), dk=((B, Hkv, Sk, Dqk), q.dtype, False),
+                dv=((B, Hkv, Sk, Dv), q.dtype, False), lse=((B, Hq, S), f32, True), delta=((B, Hq, S), f32, True),
+                sink=((Hq,), f32, True), dsink=((Hq,), f32, True), cu_seqlens=(None, torch.int32, True),
+                cu_seqlens_k=(None, torch.int32, True))
+    for name, t in named.items():
+        if t is None:
+            continue
+        shape, dtype, contiguous = want[name]
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if shape is None:  # sequence offsets: nseq + 1 entries
+            if t.dim() != 1 or t.numel() < 2:
+                raise ValueError(f"{name} must be 1-D with at least two offsets")
+        elif tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+        if contiguous and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    cu, cuk = named.get("cu_seqlens"), named.get("cu_seqlens_k")
+    if cuk is not None and (cu is None or cuk.numel() != cu.numel()):
+        raise ValueError("cu_seqlens_k needs cu_seqlens with as many offsets")
+
+
 def _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, group_mode=GQA_GROUP_TMEM,
             red_mode=None, deterministic=False, cu_seqlens_k=None, max_seqlen_k=None, window_right=0, **tensors):
     """`tensors`: any of o, do, dq, dk, dv whose layouts the call uses.  k / v may have another
@@ -76,6 +114,7 @@ def attention_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, caus
                       cu_seqlens_k: Optional[torch.Tensor] = None, max_seqlen_k: Optional[int] = None,
                       window_right: int = 0, workspace: Optional[torch.Tensor] = None):
     """Returns (o, lse): o [B,Hq,S,Dv] in q's dtype, lse [B,Hq,S] fp32 (natural log, sink included)."""
+    _validate(q, k, v, sink=sink, cu_seqlens=cu_seqlens, cu_seqlens_k=cu_seqlens_k)
     B, Hq, S, _ = q.shape
     o = _empty_like_layout(q, v.shape[3])
     p = _params(q, k, v, causal, window, scale, cu_seqlens, max_seqlen, cu_seqlens_k=cu_seqlens_k,
@@ -96,9 +135,11 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                        out: Optional[dict] = None) -> dict:
     """Returns dict(dq, dk, dv, delta[, dsink]).  `out` may hold preallocated tensors of the same names.
     red_mode None picks :func:`preferred_red_mode`."""
+    res = dict(out) if out else {}
+    _validate(q, k, v, o=o, do=dout, lse=lse, sink=sink, cu_seqlens=cu_seqlens, cu_seqlens_k=cu_seqlens_k,
+              **{n: t for n, t in res.items() if n in ("dq", "dk", "dv", "delta", "dsink")})
     B, Hq, S, Dqk = q.shape
     Hkv, Dv = k.shape[1], v.shape[3]
-    res = dict(out) if out else {}
     dev = q.device
     if "dq" not in res:
         res["dq"] = _empty_like_layout(q, Dqk)
